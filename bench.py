@@ -1,0 +1,362 @@
+"""Benchmark of the VC-Attention hot path on GB300.
+
+One step = the whole path over one batch: vca_group (k-means + permutation) ->
+vca_prep_quant (fused V-Smooth prep) -> vca_attention (FP8 attention with
+ExpCast and the mean restore), on the Wan2.2-14B-shaped video self-attention
+workload (B=1, H=40, N=70,656, d=128, k=64, 8 k-means rounds).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload wan|wan_exp|nvfp4|tiny] [--N n]
+
+`value` = attention FLOP (4 B H N^2 d) per second of the whole step, inputs
+resident in device memory; `e2e` = the same with the step's inputs copied from
+pinned host memory and the output copied back inside the timed region.
+`--impl reference` times the CPU oracle on the host cores instead (a bounded
+sample of the same workload per step, extrapolated).  Under torchrun every rank
+runs its own replica of the workload (the path shards by (batch, head) with no
+exchange); the max time over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="wan")
+    ap.add_argument("--N", type=int, default=0, help="override the sequence length")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = max(mx, float(parts[2]))
+            except ValueError:
+                continue
+            for name, flag in zip(names, parts[5:9]):
+                if flag.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except (OSError, ValueError):
+        return None
+
+
+def attention_traffic(nb_ratio: float):
+    """DRAM bytes per attention launch from the committed ncu summary, scaled to
+    this workload; None when the kernel source changed since the capture."""
+    path = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    src = os.path.join(ROOT, "bit_attention_video_smooth_gb300", "csrc", "vca_attention.cu")
+    try:
+        rec = json.load(open(path))
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
+        if rec.get("kernel_sha256") != h:
+            return None
+        return rec["dram_bytes_per_launch"] * nb_ratio / rec.get("units", 1.0)
+    except (OSError, ValueError, KeyError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (cpu_baseline and --impl reference)
+# ---------------------------------------------------------------------------
+def oracle_sample(w, seed: int = 0):
+    """Time the oracle on a bounded sample of workload `w`; returns (seconds
+    extrapolated to one whole step, cores, description)."""
+    import numpy as np
+    import oracle
+    from bit_attention_video_smooth_gb300 import inputs as I
+
+    cores = os.cpu_count() or 1
+    oracle.build()
+    heads = max(1, min(w.BH, cores))
+    rows_per_head = 64
+    sub = I.with_n(w, w.N, H=heads, B=1)
+    q, k, v = (I.to_u16(t).reshape(heads, w.N, 128) for t in I.make_qkv(sub, seed=seed))
+    rows = I.sample_rows(w.N, rows_per_head, seed=seed).numpy()
+    t0 = time.perf_counter()
+    _, perm, _, _ = oracle.group(v, w.k, w.iters)
+    t1 = time.perf_counter()
+    vmode = oracle.V_NVFP4 if w.vmode == "nvfp4" else oracle.V_E4M3
+    pre = oracle.prep(q, k, v, perm, vmode=vmode)
+    t2 = time.perf_counter()
+    mode = oracle.P_NVFP4 if w.vmode == "nvfp4" else (oracle.P_EXPCAST if w.expcast else oracle.P_EXP)
+    oracle.attention(pre, mode, rows=rows)
+    t3 = time.perf_counter()
+    reps = w.BH / heads
+    full = (t1 - t0) * reps + (t2 - t1) * reps + (t3 - t2) * reps * (w.N / rows.size)
+    desc = (f"oracle on {heads} of {w.BH} heads: group+prep in full, attention on {rows.size} of {w.N} "
+            f"query rows per head; extrapolated x{reps:.2f} heads, x{w.N / rows.size:.1f} rows")
+    return full, cores, desc, (t3 - t0)
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (replicas: barrier + max over ranks only)
+# ---------------------------------------------------------------------------
+def dist_setup():
+    import torch
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return ws, rank, local
+
+
+def dist_max(x: float, ws: int) -> float:
+    if ws == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def dist_barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+def run_reference(args, w, ws, rank):
+    if rank != 0:
+        return
+    for _ in range(args.warmup):
+        oracle_sample(w, seed=1)
+    times, cores, desc = [], 1, ""
+    for i in range(args.steps):
+        full, cores, desc, _ = oracle_sample(w, seed=2 + i)
+        times.append(full)
+    t = statistics.mean(times)
+    value = w.flops / t / 1e12
+    line = {
+        "impl": "reference", "metric": "VC-attention TFLOP/s (group + prep + attention step)",
+        "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64/f32 (oracle)", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k, "iters": w.iters,
+                   "vmode": w.vmode, "expcast": w.expcast},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, w, ws, rank, local):
+    import torch
+    from bit_attention_video_smooth_gb300 import inputs as I
+    from bit_attention_video_smooth_gb300 import vca
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    vmode = vca.VCA_V_NVFP4 if w.vmode == "nvfp4" else vca.VCA_V_E4M3
+    Q, K, V = I.make_qkv(w, seed=1234 + rank, device=dev)
+    g = vca.alloc_group(w.B, w.H, w.N, w.k, dev)
+    p = vca.alloc_prep(w.B, w.H, w.N, vmode, dev)
+    O = torch.empty((w.B, w.H, w.N, 128), dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def step(marks=None):
+        if marks:
+            marks[0].record(stream)
+        vca.vca_group(V, w.k, w.iters, g.labels, g.perm, g.counts, g.centroids, g.ws)
+        if marks:
+            marks[1].record(stream)
+        vca.vca_prep_quant(Q, K, V, g.perm, vmode, p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale,
+                           p.v_mean, p.ws)
+        if marks:
+            marks[2].record(stream)
+        vca.vca_attention(p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean, w.B, w.H, w.N, 128,
+                          0.0, int(w.expcast), vmode, O, status)
+        if marks:
+            marks[3].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} after warm-up")
+
+    # inputs (Q, K, V: 3 x BH N d bf16) exceed the 129 MB L2, so no flush is needed between steps
+    marks = [[ev() for _ in range(4)] for _ in range(args.steps)]
+    start, stop = ev(), ev()
+    dist_barrier(ws)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        start.record(stream)
+        for i in range(args.steps):
+            step(marks[i])
+        stop.record(stream)
+        torch.cuda.synchronize()
+    dist_barrier(ws)
+    ms_total = start.elapsed_time(stop)
+    t_group = statistics.mean(m[0].elapsed_time(m[1]) for m in marks)
+    t_prep = statistics.mean(m[1].elapsed_time(m[2]) for m in marks)
+    t_attn = statistics.mean(m[2].elapsed_time(m[3]) for m in marks)
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())} in the timed region")
+    ms_step = dist_max(ms_total / args.steps, ws)
+    value = ws * w.flops / (ms_step * 1e-3) / 1e12
+
+    # end to end through the public API: pinned host inputs in, O back to the host
+    e2e = None
+    if not args.no_e2e:
+        hQ, hK, hV = (t.cpu().pin_memory() for t in (Q, K, V))
+        hO = torch.empty(O.shape, dtype=O.dtype, pin_memory=True)
+        dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+
+        def e2e_step():
+            dQ.copy_(hQ, non_blocking=True)
+            dK.copy_(hK, non_blocking=True)
+            dV.copy_(hV, non_blocking=True)
+            vca.vca_group(dV, w.k, w.iters, g.labels, g.perm, g.counts, g.centroids, g.ws)
+            vca.vca_prep_quant(dQ, dK, dV, g.perm, vmode, p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale,
+                               p.v_mean, p.ws)
+            vca.vca_attention(p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean, w.B, w.H, w.N, 128,
+                              0.0, int(w.expcast), vmode, O, status)
+            hO.copy_(O, non_blocking=True)
+
+        for _ in range(max(3, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        es, ee = ev(), ev()
+        dist_barrier(ws)
+        es.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        ee.record(stream)
+        torch.cuda.synchronize()
+        ms_e2e = dist_max(es.elapsed_time(ee) / args.steps, ws)
+        h2d = sum(t.numel() * t.element_size() for t in (hQ, hK, hV))
+        e2e = {"value": ws * w.flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hO.numel() * hO.element_size()}
+
+    peaks = load_peaks()
+    if peaks and "bf16_tflops_sustained" in peaks:
+        peak = 2.0 * peaks["bf16_tflops_sustained"]
+        peak_note = "measured: 2 x sustained cuBLAS bf16 (FP8 / bf16 nominal ratio 4.5 / 2.25)"
+    else:
+        peak = 2.0 * 1700.0
+        peak_note = "fallback: 2 x 1.7 PF sustained bf16"
+    achieved = w.flops / (t_attn * 1e-3) / 1e12
+    traffic = attention_traffic(1.0)
+    line = {
+        "metric": "VC-attention TFLOP/s (group + prep + attention step)", "value": value, "unit": "TFLOP/s",
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if vmode == 0 else "e4m3/e2m1",
+        "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k, "iters": w.iters,
+                   "vmode": w.vmode, "expcast": w.expcast, "parallelism": f"replicas x{ws}",
+                   "l2": "inputs (3 x 724 MB) exceed L2; no flush"},
+        "breakdown_ms": {"group": t_group, "prep": t_prep, "attention": t_attn},
+        "attention_tflops": achieved,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
+                     "kernel": "attention_e4m3_kernel"},
+        "gpu_launches": args.steps * (1 + 2 * w.iters + 1 + 3 + 1),
+        "clocks": clocks.summary(),
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu_baseline:
+        full, cores, desc, wall = oracle_sample(w)
+        line["cpu_baseline"] = {"value": w.flops / full / 1e12, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                                "sample": desc, "sample_wall_s": wall}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    from bit_attention_video_smooth_gb300 import inputs as I
+    w = I.WORKLOADS[args.workload]
+    if args.N:
+        w = I.with_n(w, args.N)
+    ws, rank, local = dist_setup()
+    if args.impl == "reference":
+        run_reference(args, w, ws, rank)
+    else:
+        run_ours(args, w, ws, rank, local)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

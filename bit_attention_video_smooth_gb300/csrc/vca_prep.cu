@@ -1,0 +1,261 @@
+// vca_prep.cu -- the fused V-Smooth prep ("VC-Attention", paper page, section
+// "method": each 128-token hardware block subtracts its own mean, stored as a
+// 16-bit vector, and only the residual is quantised -- per-channel E4M3 for the
+// 8-bit path, NVFP4 for the 4-bit path; the preprocessing chain is fused so no
+// high-precision intermediate goes back to device memory).
+//
+// A per-channel residual scale over the whole sequence needs the sequence-wide
+// amax before any residual byte can be written, so the prep is three launches:
+//   prep_stats  grid (nb, BH): Q and K blocks (K gathered by perm) -> FP8 with a
+//               per-block absmax scale; the gathered V block -> its bf16 mean and
+//               the per-channel amax of the residual (a small partial);
+//   prep_scale  grid (BH): reduce the partials -> per-channel scales (E4M3) or
+//               the per-(b,h) scale (NVFP4);
+//   prep_vquant grid (nb, BH): gather V again (L2-resident when a head's blocks
+//               run close together), subtract the stored mean, quantise, and
+//               write the residual channel-major (tokens contiguous per channel,
+//               the K-major operand layout of the PV contraction).
+#include "vca_device.cuh"
+#include "vca_internal.h"
+
+namespace vca {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kRowPad = 8;                      // bf16 pad per token row of the V tile
+constexpr int kRowStride = kD + kRowPad;
+
+__device__ __forceinline__ float block_max(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) red[w] = v;
+    __syncthreads();
+    float r = red[0];
+    for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, red[i]);
+    return r;
+}
+
+// Quantise one 128 x 128 bf16 block (rows given by `rows`, or contiguous from
+// `row0` when rows == nullptr) to E4M3 with the block's absmax scale.
+__device__ __forceinline__ void quant_qk_block(const uint16_t *__restrict__ X, int64_t head_row0,
+                                               const int32_t *__restrict__ rows, int row0, uint8_t *__restrict__ out,
+                                               float *__restrict__ scale, float *red) {
+    const int tid = threadIdx.x;
+    uint4 v[8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int u = i * kThreads + tid;
+        const int r = u >> 4, c8 = (u & 15) * 8;
+        const int64_t src = head_row0 + (rows ? rows[r] : row0 + r);
+        v[i] = *reinterpret_cast<const uint4 *>(X + src * kD + c8);
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&v[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+        }
+    }
+    amax = block_max(amax, red);
+    float inv = 1.0f, s = 1.0f;
+    if (amax > 0.0f) {
+        inv = __fdiv_rn(448.0f, amax);
+        s = __fdiv_rn(amax, 448.0f);
+    }
+    if (tid == 0) *scale = s;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int u = i * kThreads + tid;
+        const uint32_t *w = reinterpret_cast<const uint32_t *>(&v[i]);
+        uint32_t packed[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t a = e4m3x2(__fmul_rn(__uint_as_float(w[2 * j] << 16), inv),
+                                      __fmul_rn(__uint_as_float(w[2 * j] & 0xFFFF0000u), inv));
+            const uint32_t b = e4m3x2(__fmul_rn(__uint_as_float(w[2 * j + 1] << 16), inv),
+                                      __fmul_rn(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), inv));
+            packed[j] = a | (b << 16);
+        }
+        *reinterpret_cast<uint2 *>(out + static_cast<int64_t>(u) * 8) = make_uint2(packed[0], packed[1]);
+    }
+}
+
+// Gather the block's 128 V rows into shared memory (token-major, padded rows).
+__device__ __forceinline__ void load_v_tile(const uint16_t *__restrict__ V, int64_t head_row0,
+                                            const int32_t *__restrict__ rows, uint16_t *sV) {
+    for (int u = threadIdx.x; u < kBlk * kD / 8; u += kThreads) {
+        const int r = u >> 4, c8 = (u & 15) * 8;
+        *reinterpret_cast<uint4 *>(sV + r * kRowStride + c8) =
+            *reinterpret_cast<const uint4 *>(V + (head_row0 + rows[r]) * kD + c8);
+    }
+}
+
+// Error-free transformation: a + b = s + e exactly (Knuth's two-sum).
+__device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
+    s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+
+__global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__restrict__ Q,
+                                                              const uint16_t *__restrict__ K,
+                                                              const uint16_t *__restrict__ V,
+                                                              const int32_t *__restrict__ perm, int N,
+                                                              uint8_t *__restrict__ q8, float *__restrict__ sq,
+                                                              uint8_t *__restrict__ k8, float *__restrict__ sk,
+                                                              uint16_t *__restrict__ v_mean,
+                                                              float *__restrict__ amax_part) {
+    __shared__ __align__(16) uint16_t sV[kBlk * kRowStride];
+    __shared__ float red[kThreads / 32];
+    const int b = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
+    const int64_t head_row0 = static_cast<int64_t>(bh) * N;
+    const int32_t *rows = perm + head_row0 + static_cast<int64_t>(b) * kBlk;
+    const int64_t blk_off = (head_row0 + static_cast<int64_t>(b) * kBlk) * kD;
+
+    quant_qk_block(Q, head_row0, nullptr, b * kBlk, q8 + blk_off, sq + static_cast<int64_t>(bh) * nb + b, red);
+    quant_qk_block(K, head_row0, rows, 0, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b, red);
+
+    load_v_tile(V, head_row0, rows, sV);
+    __syncthreads();
+    const int ch = threadIdx.x;
+    if (ch < kD) {
+        // block mean: compensated fp32 sum (the rounded exact sum), / 128, -> bf16
+        float s = 0.0f, comp = 0.0f;
+        for (int t = 0; t < kBlk; ++t) {
+            float e;
+            two_sum(s, bf16_bits_to_f32(sV[t * kRowStride + ch]), s, e);
+            comp = __fadd_rn(comp, e);
+        }
+        const float mean = __fdiv_rn(__fadd_rn(s, comp), 128.0f);
+        const __nv_bfloat16 mu = __float2bfloat16_rn(mean);
+        const float muf = __bfloat162float(mu);
+        v_mean[(static_cast<int64_t>(bh) * nb + b) * kD + ch] = __bfloat16_as_ushort(mu);
+        float a = 0.0f;
+        for (int t = 0; t < kBlk; ++t)
+            a = fmaxf(a, fabsf(__fsub_rn(bf16_bits_to_f32(sV[t * kRowStride + ch]), muf)));
+        amax_part[(static_cast<int64_t>(bh) * nb + b) * kD + ch] = a;
+    }
+}
+
+// E4M3: per channel a_c -> v_scale = a_c / 448, inv_c = 448 / a_c.
+// NVFP4: g = max_c a_c / (6 * 448) -> v_scale[bh]; inv[bh][0] = 6 g, inv[bh][1] = g.
+__global__ void __launch_bounds__(kD) prep_scale_kernel(int nb, int vmode, const float *__restrict__ amax_part,
+                                                        float *__restrict__ v_scale, float *__restrict__ inv) {
+    __shared__ float red[kD / 32];
+    const int bh = blockIdx.x, ch = threadIdx.x;
+    float a = 0.0f;
+    for (int b = 0; b < nb; ++b) a = fmaxf(a, amax_part[(static_cast<int64_t>(bh) * nb + b) * kD + ch]);
+    if (vmode == 0) {
+        float s = 1.0f, iv = 1.0f;
+        if (a > 0.0f) { s = __fdiv_rn(a, 448.0f); iv = __fdiv_rn(448.0f, a); }
+        v_scale[static_cast<int64_t>(bh) * kD + ch] = s;
+        inv[static_cast<int64_t>(bh) * kD + ch] = iv;
+    } else {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        if ((ch & 31) == 0) red[ch >> 5] = a;
+        __syncthreads();
+        if (ch == 0) {
+            float m = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+            const float g = (m > 0.0f) ? __fdiv_rn(m, 2688.0f) : 1.0f;   // 6 * 448
+            v_scale[bh] = g;
+            inv[static_cast<int64_t>(bh) * kD + 0] = __fmul_rn(6.0f, g);
+            inv[static_cast<int64_t>(bh) * kD + 1] = g;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) prep_vquant_kernel(const uint16_t *__restrict__ V,
+                                                               const int32_t *__restrict__ perm, int N, int vmode,
+                                                               const uint16_t *__restrict__ v_mean,
+                                                               const float *__restrict__ inv,
+                                                               uint8_t *__restrict__ v_res,
+                                                               uint8_t *__restrict__ v_sf) {
+    __shared__ __align__(16) uint16_t sV[kBlk * kRowStride];
+    const int b = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
+    const int64_t head_row0 = static_cast<int64_t>(bh) * N;
+    const int32_t *rows = perm + head_row0 + static_cast<int64_t>(b) * kBlk;
+    load_v_tile(V, head_row0, rows, sV);
+    __syncthreads();
+    const int ch = threadIdx.x & (kD - 1);
+    const int half = threadIdx.x >> 7;                  // tokens 64*half .. 64*half+63
+    const float muf = bf16_bits_to_f32(v_mean[(static_cast<int64_t>(bh) * nb + b) * kD + ch]);
+    const int64_t cb = (static_cast<int64_t>(bh) * nb + b) * kD + ch;   // (block, channel) index
+    if (vmode == 0) {
+        const float iv = inv[static_cast<int64_t>(bh) * kD + ch];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int t0 = half * 64 + g * 16;
+            uint32_t w[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float r[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    r[q] = __fmul_rn(__fsub_rn(bf16_bits_to_f32(sV[(t0 + 4 * j + q) * kRowStride + ch]), muf), iv);
+                w[j] = e4m3x2(r[0], r[1]) | (e4m3x2(r[2], r[3]) << 16);
+            }
+            *reinterpret_cast<uint4 *>(v_res + cb * kBlk + t0) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    } else {
+        const float g6 = inv[static_cast<int64_t>(bh) * kD + 0];
+        const float gs = inv[static_cast<int64_t>(bh) * kD + 1];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+            const int t0 = half * 64 + g * 16;
+            float r[16];
+            float a16 = 0.0f;
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                r[q] = __fsub_rn(bf16_bits_to_f32(sV[(t0 + q) * kRowStride + ch]), muf);
+                a16 = fmaxf(a16, fabsf(r[q]));
+            }
+            const uint32_t sf = e4m3(__fdiv_rn(a16, g6));
+            float iv = 0.0f;
+            if (sf != 0) iv = __fdiv_rn(1.0f, __fmul_rn(e4m3_to_f32(sf), gs));
+            uint32_t w[2] = {0u, 0u};
+#pragma unroll
+            for (int q = 0; q < 16; q += 2) {
+                const uint32_t byte = e2m1x2(__fmul_rn(r[q], iv), __fmul_rn(r[q + 1], iv)) & 0xFFu;
+                w[q >> 3] |= byte << (8 * ((q >> 1) & 3));
+            }
+            *reinterpret_cast<uint2 *>(v_res + cb * (kBlk / 2) + t0 / 2) = make_uint2(w[0], w[1]);
+            v_sf[cb * (kBlk / 16) + t0 / 16] = static_cast<uint8_t>(sf);
+        }
+    }
+}
+
+}  // namespace
+
+PrepWorkspace prep_workspace_layout(int BH, int N) {
+    PrepWorkspace w;
+    const size_t nb = static_cast<size_t>(N) / kBlk;
+    w.off_amax = 0;
+    const size_t amax_bytes = (sizeof(float) * BH * nb * kD + 255) & ~size_t(255);
+    w.off_inv = amax_bytes;
+    w.bytes = amax_bytes + ((sizeof(float) * BH * kD + 255) & ~size_t(255));
+    return w;
+}
+
+cudaError_t launch_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int BH, int N,
+                        int vmode, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res, uint8_t *v_sf,
+                        float *v_scale, uint16_t *v_mean, void *ws, cudaStream_t st) {
+    const PrepWorkspace w = prep_workspace_layout(BH, N);
+    unsigned char *base = static_cast<unsigned char *>(ws);
+    float *amax = reinterpret_cast<float *>(base + w.off_amax);
+    float *inv = reinterpret_cast<float *>(base + w.off_inv);
+    const int nb = N / kBlk;
+    prep_stats_kernel<<<dim3(nb, BH), kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prep_scale_kernel<<<BH, kD, 0, st>>>(nb, vmode, amax, v_scale, inv);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    prep_vquant_kernel<<<dim3(nb, BH), kThreads, 0, st>>>(V, perm, N, vmode, v_mean, inv, v_res, v_sf);
+    return cudaGetLastError();
+}
+
+}  // namespace vca

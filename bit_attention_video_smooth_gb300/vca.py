@@ -1,0 +1,226 @@
+"""Thin ctypes binding of ``libvca.so`` (the C ABI in ``include/vca.h``).
+
+The functions keep the C entry points' names and only marshal arguments:
+PyTorch tensors provide device memory and the current CUDA stream; every step
+of the computation runs in the library's CUDA kernels.  If the library has not
+been built (``__graft_entry__.build()`` or ``python
+bit_attention_video_smooth_gb300/build.py``) importing this module raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libvca.so")
+
+VCA_OK, VCA_ERR_INVALID_ARG, VCA_ERR_UNSUPPORTED, VCA_ERR_CUDA, VCA_ERR_TIMEOUT, VCA_ERR_WORKSPACE = range(6)
+VCA_V_E4M3, VCA_V_NVFP4 = 0, 1
+VCA_OP_GROUP, VCA_OP_PREP, VCA_OP_ATTENTION = 0, 1, 2
+
+# Entry points declared in include/vca.h (the ABI test checks they are exported).
+EXPORTS = ("vca_status_string", "vca_version", "vca_workspace_bytes", "vca_group", "vca_prep_quant",
+           "vca_attention", "vca_expcast_codes", "vca_e4m3_encode_bits", "vca_selftest_timeout",
+           "vca_set_wait_limit_ns")
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libvca.so is not built ({LIB_PATH}); run __graft_entry__.build() -- "
+                      "there is no fallback implementation")
+
+_lib = ctypes.CDLL(LIB_PATH)
+_P, _I, _I64, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_size_t
+_SIGS = {
+    "vca_status_string": (ctypes.c_char_p, [_I]),
+    "vca_version": (_I, []),
+    "vca_workspace_bytes": (_SZ, [_I] * 7),
+    "vca_group": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "vca_prep_quant": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "vca_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P]),
+    "vca_expcast_codes": (_I, [_P, _P, _P, _I64, _P, _P]),
+    "vca_e4m3_encode_bits": (_I, [ctypes.c_uint32, _I64, _P, _P]),
+    "vca_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
+    "vca_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+}
+for _name, (_res, _args) in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.restype = _res
+    _fn.argtypes = _args
+
+
+class VCAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {vca_status_string(status)} ({status})")
+
+
+def vca_status_string(status: int) -> str:
+    return _lib.vca_status_string(int(status)).decode()
+
+
+def vca_version() -> int:
+    return int(_lib.vca_version())
+
+
+def vca_workspace_bytes(op: int, B: int, H: int, N: int, d: int = 128, k: int = 1, vmode: int = 0) -> int:
+    return int(_lib.vca_workspace_bytes(op, B, H, N, d, k, vmode))
+
+
+def vca_set_wait_limit_ns(limit_ns: int) -> None:
+    _lib.vca_set_wait_limit_ns(int(limit_ns))
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensor expected")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensor expected")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str) -> None:
+    if status != VCA_OK:
+        raise VCAError(status, where)
+
+
+def _u16(t: torch.Tensor) -> torch.Tensor:
+    return t.view(torch.int16) if t.dtype == torch.bfloat16 else t
+
+
+# ---------------------------------------------------------------------------
+# Entry points (same names as the C ABI)
+# ---------------------------------------------------------------------------
+def vca_group(V: torch.Tensor, k: int, iters: int, labels: torch.Tensor, perm: torch.Tensor,
+              counts: Optional[torch.Tensor], centroids: Optional[torch.Tensor], ws: torch.Tensor,
+              stream=None) -> None:
+    B, H, N, d = V.shape
+    st = _lib.vca_group(_ptr(_u16(V)), B, H, N, d, k, iters, _ptr(labels), _ptr(perm), _ptr(counts),
+                        _ptr(centroids), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "vca_group")
+
+
+def vca_prep_quant(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, ws,
+                   stream=None) -> None:
+    B, H, N, d = Q.shape
+    st = _lib.vca_prep_quant(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode,
+                             _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
+                             _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "vca_prep_quant")
+
+
+def vca_attention(q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, B: int, H: int, N: int, d: int,
+                  softmax_scale: float, expcast: int, vmode: int, O, dev_status=None, stream=None) -> None:
+    st = _lib.vca_attention(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
+                            _ptr(_u16(v_mean)), B, H, N, d, float(softmax_scale), int(expcast), int(vmode),
+                            _ptr(_u16(O)), _ptr(dev_status), _stream(stream))
+    _check(st, "vca_attention")
+
+
+def vca_expcast_codes(s_raw, c, m, out, stream=None) -> None:
+    _check(_lib.vca_expcast_codes(_ptr(s_raw), _ptr(c), _ptr(m), s_raw.numel(), _ptr(out), _stream(stream)),
+           "vca_expcast_codes")
+
+
+def vca_e4m3_encode_bits(start: int, n: int, out, stream=None) -> None:
+    _check(_lib.vca_e4m3_encode_bits(ctypes.c_uint32(start), n, _ptr(out), _stream(stream)), "vca_e4m3_encode_bits")
+
+
+def vca_selftest_timeout(dev_status, limit_ns: int, stream=None) -> None:
+    _check(_lib.vca_selftest_timeout(_ptr(dev_status), ctypes.c_uint64(limit_ns), _stream(stream)),
+           "vca_selftest_timeout")
+
+
+# ---------------------------------------------------------------------------
+# Buffer sets and the whole path (allocation through PyTorch)
+# ---------------------------------------------------------------------------
+@dataclass
+class Grouped:
+    labels: torch.Tensor
+    perm: torch.Tensor
+    counts: torch.Tensor
+    centroids: torch.Tensor
+    ws: torch.Tensor
+
+
+@dataclass
+class Prepared:
+    q8: torch.Tensor
+    sq: torch.Tensor
+    k8: torch.Tensor
+    sk: torch.Tensor
+    v_res: torch.Tensor
+    v_sf: Optional[torch.Tensor]
+    v_scale: torch.Tensor
+    v_mean: torch.Tensor
+    ws: torch.Tensor
+    vmode: int
+
+
+def alloc_group(B, H, N, k, device="cuda") -> Grouped:
+    BH = B * H
+    ws = torch.empty(max(16, vca_workspace_bytes(VCA_OP_GROUP, B, H, N, 128, k, 0)), dtype=torch.uint8, device=device)
+    return Grouped(torch.empty((BH, N), dtype=torch.int32, device=device),
+                   torch.empty((BH, N), dtype=torch.int32, device=device),
+                   torch.empty((BH, k), dtype=torch.int32, device=device),
+                   torch.empty((BH, k, 128), dtype=torch.float32, device=device), ws)
+
+
+def alloc_prep(B, H, N, vmode=VCA_V_E4M3, device="cuda") -> Prepared:
+    BH, nb, d = B * H, N // 128, 128
+    ws = torch.empty(max(16, vca_workspace_bytes(VCA_OP_PREP, B, H, N, d, 1, vmode)), dtype=torch.uint8, device=device)
+    if vmode == VCA_V_E4M3:
+        v_res = torch.empty((BH, nb, d, 128), dtype=torch.uint8, device=device)
+        v_sf = None
+        v_scale = torch.empty((BH, d), dtype=torch.float32, device=device)
+    else:
+        v_res = torch.empty((BH, nb, d, 64), dtype=torch.uint8, device=device)
+        v_sf = torch.empty((BH, nb, d, 8), dtype=torch.uint8, device=device)
+        v_scale = torch.empty((BH,), dtype=torch.float32, device=device)
+    return Prepared(torch.empty((BH, N, d), dtype=torch.uint8, device=device),
+                    torch.empty((BH, nb), dtype=torch.float32, device=device),
+                    torch.empty((BH, N, d), dtype=torch.uint8, device=device),
+                    torch.empty((BH, nb), dtype=torch.float32, device=device),
+                    v_res, v_sf, v_scale,
+                    torch.empty((BH, nb, d), dtype=torch.bfloat16, device=device), ws, vmode)
+
+
+def group(V: torch.Tensor, k: int, iters: int, out: Optional[Grouped] = None) -> Grouped:
+    B, H, N, _ = V.shape
+    g = out or alloc_group(B, H, N, k, V.device)
+    vca_group(V, k, iters, g.labels, g.perm, g.counts, g.centroids, g.ws)
+    return g
+
+
+def prep_quant(Q, K, V, perm, vmode=VCA_V_E4M3, out: Optional[Prepared] = None) -> Prepared:
+    B, H, N, _ = Q.shape
+    p = out or alloc_prep(B, H, N, vmode, Q.device)
+    vca_prep_quant(Q, K, V, perm, vmode, p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean, p.ws)
+    return p
+
+
+def attention(p: Prepared, B: int, H: int, N: int, expcast: bool = True, softmax_scale: float = 0.0,
+              out: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    O = out if out is not None else torch.empty((B, H, N, 128), dtype=torch.bfloat16, device=p.q8.device)
+    vca_attention(p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean, B, H, N, 128,
+                  softmax_scale, int(expcast), p.vmode, O, dev_status)
+    return O
+
+
+def vc_attention(Q, K, V, k: int = 64, iters: int = 8, expcast: bool = True, vmode: int = VCA_V_E4M3,
+                 softmax_scale: float = 0.0):
+    """The whole hot path: group -> prep -> attention.  Returns (O, grouped, prepared)."""
+    B, H, N, _ = Q.shape
+    g = group(V, k, iters)
+    p = prep_quant(Q, K, V, g.perm, vmode)
+    O = attention(p, B, H, N, expcast=expcast, softmax_scale=softmax_scale)
+    return O, g, p

@@ -1,0 +1,89 @@
+"""The C-ABI library loads on a machine without a GPU, exports every entry point
+declared in include/vca.h, and rejects bad arguments synchronously (before any
+CUDA call) with the documented status codes."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from bit_attention_video_smooth_gb300 import build
+    path = build.build()
+    return ctypes.CDLL(path)
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "vca.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(vca_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert "vca_group" in names and "vca_prep_quant" in names and "vca_attention" in names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_binding_lists_every_export():
+    from bit_attention_video_smooth_gb300 import vca
+    assert sorted(vca.EXPORTS) == _declared()
+
+
+def test_status_strings_and_version(lib):
+    lib.vca_status_string.restype = ctypes.c_char_p
+    assert lib.vca_status_string(0) == b"ok"
+    assert lib.vca_status_string(4) == b"device wait timed out"
+    assert lib.vca_status_string(99) == b"unknown status"
+    assert lib.vca_version() >= 100
+
+
+def test_workspace_sizes(lib):
+    lib.vca_workspace_bytes.restype = ctypes.c_size_t
+    ws = lib.vca_workspace_bytes
+    assert ws(0, 1, 40, 70656, 128, 64, 0) > 0
+    assert ws(1, 1, 40, 70656, 128, 1, 0) > 0
+    assert ws(0, 1, 2, 1000, 128, 8, 0) == 0        # N not a multiple of 128
+    assert ws(0, 1, 2, 1024, 64, 8, 0) == 0         # d != 128
+    assert ws(0, 1, 2, 1024, 128, 0, 0) == 0        # k < 1
+    assert ws(0, 1, 2, 1024, 128, 129, 0) == 0      # k above the supported maximum
+    assert ws(2, 1, 2, 1024, 128, 8, 0) == 0        # attention needs no workspace
+
+
+def test_invalid_arguments_rejected_without_cuda(lib):
+    P = ctypes.c_void_p
+    fake = P(0x10000)                                  # aligned, never dereferenced
+    lib.vca_attention.argtypes = [P] * 8 + [ctypes.c_int] * 4 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, P, P, P]
+    # null output pointer
+    assert lib.vca_attention(*([fake] * 8), 1, 2, 1024, 128, 0.0, 1, 0, None, None, None) == 1
+    # ragged N
+    assert lib.vca_attention(*([fake] * 8), 1, 2, 1000, 128, 0.0, 1, 0, fake, None, None) == 1
+    # misaligned pointer
+    assert lib.vca_attention(P(0x10001), *([fake] * 7), 1, 2, 1024, 128, 0.0, 1, 0, fake, None, None) == 1
+    # ExpCast has no NVFP4 counterpart
+    assert lib.vca_attention(*([fake] * 8), 1, 2, 1024, 128, 0.0, 1, 1, fake, None, None) == 2
+    lib.vca_group.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                              ctypes.c_int, P, P, P, P, P, ctypes.c_size_t, P]
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 0, fake, fake, None, None, fake, 1 << 30, None) == 1  # iters
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 4, fake, fake, None, None, None, 0, None) == 5          # no ws
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 4, fake, fake, None, None, fake, 16, None) == 5         # too small
+    lib.vca_selftest_timeout.argtypes = [P, ctypes.c_uint64, P]
+    assert lib.vca_selftest_timeout(fake, 10, None) == 1
+
+
+def test_oracle_and_library_share_no_code():
+    # the oracle is plain C compiled by gcc; the library is CUDA compiled by nvcc;
+    # neither includes the other's files
+    orc = open(os.path.join(ROOT, "oracle", "vca_oracle.c")).read()
+    assert "#include \"" not in orc
+    csrc = os.path.join(ROOT, "bit_attention_video_smooth_gb300", "csrc")
+    for f in os.listdir(csrc):
+        text = open(os.path.join(csrc, f)).read()
+        assert "oracle" not in text.lower(), f
+    binding = open(os.path.join(ROOT, "bit_attention_video_smooth_gb300", "vca.py")).read()
+    assert "import oracle" not in binding and "from oracle" not in binding

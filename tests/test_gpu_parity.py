@@ -1,0 +1,238 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.
+
+Bars: ExpCast codes, E4M3 conversions, cluster labels on well-separated inputs
+and the permutation bit-exact; FP8 Q/K bytes and scales exact; E4M3 residual
+bytes >= 99.99% identical, the rest one code apart; attention output within
+relative L2 <= 1e-3 and max-abs <= 4e-3 * max|O| of the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_attention_video_smooth_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-3
+MAX_ABS = 4e-3
+
+
+@pytest.fixture(scope="module")
+def V():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_attention_video_smooth_gb300 import vca
+    return vca
+
+
+def _f32(u16):
+    return (np.asarray(u16, np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def _dev(a, dtype=None):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    if dtype is not None:
+        t = t.view(dtype)
+    return t.cuda()
+
+
+def _o_close(got_u16, ref_u16):
+    g = _f32(got_u16).astype(np.float64)
+    r = _f32(ref_u16).astype(np.float64)
+    rel = np.linalg.norm(g - r) / max(np.linalg.norm(r), 1e-30)
+    mx = np.abs(g - r).max() / max(np.abs(r).max(), 1e-30)
+    return rel, mx
+
+
+# ---------------------------------------------------------------------------
+# formats and the ExpCast map
+# ---------------------------------------------------------------------------
+def test_expcast_codes_bit_exact(V, orc):
+    rng = np.random.default_rng(11)
+    n = 1 << 20
+    s = np.concatenate([rng.standard_normal(n) * 2e4, rng.uniform(-50, 50, n)]).astype(np.float32)
+    c = np.concatenate([rng.uniform(1e-5, 1e-3, n), rng.uniform(0.01, 2, n)]).astype(np.float32)
+    m = (s * c).astype(np.float32) + rng.uniform(0, 12, 2 * n).astype(np.float32)   # m >= s*c mostly
+    # edge cases: t exactly at .5 boundaries, at the flush threshold, above the clip
+    edge_s = np.array([0.0, 0.0, 0.0, 1.0, -1.0, 20.0, np.inf, -np.inf, np.nan, 1e30], np.float32)
+    edge_c = np.ones_like(edge_s)
+    edge_m = np.array([0.0, 6.01875, 6.0187, -10.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0], np.float32)
+    s, c, m = (np.concatenate([a, b]) for a, b in ((s, edge_s), (c, edge_c), (m, edge_m)))
+    ref = orc.expcast_codes(s, c, m)
+    out = torch.empty(s.size, dtype=torch.uint8, device="cuda")
+    V.vca_expcast_codes(_dev(s), _dev(c), _dev(m), out)
+    got = out.cpu().numpy()
+    assert np.array_equal(got, ref), np.flatnonzero(got != ref)[:10]
+
+
+def test_e4m3_hardware_conversion_matches_oracle_everywhere(V, orc):
+    # every non-NaN fp32 bit pattern, in chunks
+    step = 1 << 28
+    out = torch.empty(step, dtype=torch.uint8, device="cuda")
+    for start in range(0, 1 << 32, step):
+        V.vca_e4m3_encode_bits(start, step, out)
+        got = out.cpu().numpy()
+        ref = orc.e4m3_encode_bits(start, step)
+        u = np.arange(start, start + step, dtype=np.uint64).astype(np.uint32)
+        nan = (u & 0x7FFFFFFF) > 0x7F800000
+        assert np.array_equal(got[~nan], ref[~nan]), hex(start)
+        assert np.all((got[nan] & 0x7F) == 0x7F)
+
+
+# ---------------------------------------------------------------------------
+# group: k-means + stable permutation
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("BH,N,k,iters", [(2, 1024, 8, 10), (3, 2 * 2048 + 384, 16, 4), (1, 256, 1, 2),
+                                          (2, 2048, 64, 8), (1, 512, 128, 3)])
+def test_group_bit_exact_on_separated_clusters(V, orc, BH, N, k, iters):
+    v16 = I.make_separated_v(BH, N, 128, k, seed=BH * 7 + k)
+    ref_lab, ref_perm, ref_cnt, ref_cent = orc.group(I.to_u16(v16), k, iters)
+    g = V.group(v16.view(1, BH, N, 128).cuda(), k, iters)
+    torch.cuda.synchronize()
+    assert np.array_equal(g.labels.cpu().numpy(), ref_lab)
+    assert np.array_equal(g.perm.cpu().numpy(), ref_perm)
+    assert np.array_equal(g.counts.cpu().numpy(), ref_cnt)
+    np.testing.assert_allclose(g.centroids.cpu().numpy(), ref_cent, rtol=1e-5, atol=1e-5)
+
+
+def _check_perm_properties(labels, perm, counts, k):
+    BH, N = labels.shape
+    for bh in range(BH):
+        assert np.array_equal(np.sort(perm[bh]), np.arange(N))
+        assert np.array_equal(perm[bh], np.argsort(labels[bh], kind="stable"))
+        assert np.array_equal(counts[bh], np.bincount(labels[bh], minlength=k))
+
+
+def test_group_realistic_inputs(V, orc):
+    w = I.WORKLOADS["tiny"]
+    _, _, v = I.make_qkv(w, seed=5)
+    g = V.group(v.cuda(), w.k, w.iters)
+    torch.cuda.synchronize()
+    lab, perm, cnt, cent = (t.cpu().numpy() for t in (g.labels, g.perm, g.counts, g.centroids))
+    _check_perm_properties(lab, perm, cnt, w.k)
+    ref_lab, _, _, ref_cent = orc.group(I.to_u16(v).reshape(w.BH, w.N, 128), w.k, w.iters)
+    agree = (lab == ref_lab).mean()
+    assert agree > 0.99, agree
+    v16 = I.to_u16(v).reshape(w.BH, w.N, 128)
+    for bh in range(w.BH):
+        sse_gpu = orc.kmeans_sse(v16[bh], lab[bh], cent[bh])
+        sse_ref = orc.kmeans_sse(v16[bh], ref_lab[bh], ref_cent[bh])
+        assert sse_gpu <= sse_ref * 1.005
+
+
+# ---------------------------------------------------------------------------
+# prep
+# ---------------------------------------------------------------------------
+def _prep_inputs(BH, N, seed):
+    w = I.with_n(I.WORKLOADS["tiny"], N, H=BH)
+    q, k, v = I.make_qkv(w, seed=seed)
+    perm = I.random_perm(BH, N, seed=seed + 1)
+    return q, k, v, perm
+
+
+@pytest.mark.parametrize("BH,N,seed", [(2, 1024, 0), (3, 384, 1), (1, 128, 2), (2, 2432, 3)])
+def test_prep_e4m3_parity(V, orc, BH, N, seed):
+    q, k, v, perm = _prep_inputs(BH, N, seed)
+    ref = orc.prep(*(I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v)), perm.numpy())
+    p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_E4M3)
+    torch.cuda.synchronize()
+    assert np.array_equal(p.q8.cpu().numpy(), ref["q8"])
+    assert np.array_equal(p.k8.cpu().numpy(), ref["k8"])
+    assert np.array_equal(p.sq.cpu().numpy(), ref["sq"])
+    assert np.array_equal(p.sk.cpu().numpy(), ref["sk"])
+    vm = p.v_mean.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (vm == ref["v_mean"]).mean() >= 0.9999
+    vr = p.v_res.cpu().numpy()
+    same = (vr == ref["v_res"]).mean()
+    assert same >= 0.9999, same
+    diff = np.abs(vr.astype(np.int16) - ref["v_res"].astype(np.int16))
+    near = (diff <= 1) | ((vr & 0x7F) == (ref["v_res"] & 0x7F))     # one code, or a signed zero
+    assert near.all()
+    np.testing.assert_allclose(p.v_scale.cpu().numpy(), ref["v_scale"], rtol=1e-6)
+
+
+def test_prep_nvfp4_parity(V, orc):
+    BH, N = 2, 1024
+    q, k, v, perm = _prep_inputs(BH, N, 4)
+    ref = orc.prep(*(I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v)), perm.numpy(), vmode=orc.V_NVFP4)
+    p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_NVFP4)
+    torch.cuda.synchronize()
+    assert np.array_equal(p.q8.cpu().numpy(), ref["q8"])
+    np.testing.assert_allclose(p.v_scale.cpu().numpy(), ref["v_scale"], rtol=1e-6)
+    assert (p.v_sf.cpu().numpy() == ref["v_sf"]).mean() >= 0.9999
+    assert (p.v_res.cpu().numpy() == ref["v_res"]).mean() >= 0.9999
+
+
+# ---------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------
+def _prepped_both(V, orc, BH, N, seed):
+    """Oracle prep of seeded inputs, uploaded as the device operands."""
+    q, k, v, perm = _prep_inputs(BH, N, seed)
+    ref = orc.prep(*(I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v)), perm.numpy())
+    p = V.Prepared(_dev(ref["q8"]), _dev(ref["sq"]), _dev(ref["k8"]), _dev(ref["sk"]), _dev(ref["v_res"]), None,
+                   _dev(ref["v_scale"]), _dev(ref["v_mean"], torch.bfloat16), None, V.VCA_V_E4M3)
+    return ref, p
+
+
+@pytest.mark.parametrize("expcast", [1, 0])
+@pytest.mark.parametrize("BH,N,seed", [(2, 1024, 0), (1, 128, 1), (3, 384, 2), (1, 2304, 3), (2, 4096, 4)])
+def test_attention_parity_on_oracle_operands(V, orc, expcast, BH, N, seed):
+    ref, p = _prepped_both(V, orc, BH, N, seed)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = V.attention(p, 1, BH, N, expcast=bool(expcast), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    O_ref = orc.attention(ref, orc.P_EXPCAST if expcast else orc.P_EXP)
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(BH, N, 128), O_ref)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def test_attention_end_to_end_tiny(V, orc):
+    """Both chains from the same Q, K, V and permutation: GPU prep + attention
+    against oracle prep + attention (the tiny workload, ExpCast on)."""
+    w = I.WORKLOADS["tiny"]
+    q, k, v = I.make_qkv(w, seed=9)
+    perm = I.random_perm(w.BH, w.N, seed=10)
+    ref = orc.prep(*(I.to_u16(t).reshape(w.BH, w.N, 128) for t in (q, k, v)), perm.numpy())
+    O_ref = orc.attention(ref, orc.P_EXPCAST)
+    p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_E4M3)
+    O = V.attention(p, w.B, w.H, w.N, expcast=True)
+    torch.cuda.synchronize()
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.BH, w.N, 128), O_ref)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def test_attention_whole_path_against_exact_attention(V, orc):
+    """group -> prep -> attention on the GPU; the result stays close to exact
+    fp64 attention (the method's accuracy, reported, loosely bounded)."""
+    w = I.WORKLOADS["tiny"]
+    q, k, v = I.make_qkv(w, seed=12)
+    O, g, p = V.vc_attention(q.cuda(), k.cuda(), v.cuda(), k=w.k, iters=w.iters, expcast=True)
+    torch.cuda.synchronize()
+    ex = orc.attention_exact(*(I.to_u16(t).reshape(w.BH, w.N, 128) for t in (q, k, v)))
+    got = O.float().cpu().numpy().reshape(w.BH, w.N, 128)
+    rel = np.linalg.norm(got - ex) / np.linalg.norm(ex)
+    assert rel < 0.1, rel
+
+
+def test_nvfp4_with_expcast_is_rejected(V):
+    p = V.alloc_prep(1, 1, 256, V.VCA_V_NVFP4)
+    with pytest.raises(V.VCAError) as e:
+        V.attention(p, 1, 1, 256, expcast=True)
+    assert e.value.status == V.VCA_ERR_UNSUPPORTED
+
+
+def test_bounded_wait_reports_timeout_and_context_survives(V, orc):
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    V.vca_selftest_timeout(status, 2_000_000)          # 2 ms on a barrier nothing completes
+    torch.cuda.synchronize()
+    assert int(status.item()) == V.VCA_ERR_TIMEOUT
+    # the context is still usable
+    ref, p = _prepped_both(V, orc, 1, 256, 5)
+    O = V.attention(p, 1, 1, 256, expcast=True)
+    torch.cuda.synchronize()
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(1, 256, 128),
+                       orc.attention(ref, orc.P_EXPCAST))
+    assert rel <= REL_L2
