@@ -22,7 +22,7 @@ namespace vca {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTilePad = 2;                    // bf16 pad per transposed row (bank spread)
+constexpr int kTilePad = 4;                    // bf16 pad per transposed row: keeps 8-byte row alignment
 constexpr int kTileStride = kBlk + kTilePad;   // elements per channel row of the tile
 
 __global__ void __launch_bounds__(kBlk) group_init_kernel(const uint16_t *__restrict__ V, int N, int k,
