@@ -205,16 +205,21 @@ def test_attention_end_to_end_tiny(V, orc):
 
 
 def test_attention_whole_path_against_exact_attention(V, orc):
-    """group -> prep -> attention on the GPU; the result stays close to exact
-    fp64 attention (the method's accuracy, reported, loosely bounded)."""
+    """group -> prep -> attention on the GPU, and the oracle's own group -> prep
+    -> attention, both against exact fp64 attention: the GPU path is as accurate
+    as the method itself (the two chains may cluster a few tokens differently)."""
     w = I.WORKLOADS["tiny"]
     q, k, v = I.make_qkv(w, seed=12)
     O, g, p = V.vc_attention(q.cuda(), k.cuda(), v.cuda(), k=w.k, iters=w.iters, expcast=True)
     torch.cuda.synchronize()
-    ex = orc.attention_exact(*(I.to_u16(t).reshape(w.BH, w.N, 128) for t in (q, k, v)))
+    q16, k16, v16 = (I.to_u16(t).reshape(w.BH, w.N, 128) for t in (q, k, v))
+    ex = orc.attention_exact(q16, k16, v16)
+    _, perm, _, _ = orc.group(v16, w.k, w.iters)
+    O_orc = orc.bf16_to_f32(orc.attention(orc.prep(q16, k16, v16, perm), orc.P_EXPCAST)).astype(np.float64)
     got = O.float().cpu().numpy().reshape(w.BH, w.N, 128)
-    rel = np.linalg.norm(got - ex) / np.linalg.norm(ex)
-    assert rel < 0.1, rel
+    rel_gpu = np.linalg.norm(got - ex) / np.linalg.norm(ex)
+    rel_orc = np.linalg.norm(O_orc - ex) / np.linalg.norm(ex)
+    assert rel_gpu <= rel_orc * 1.02 + 1e-3, (rel_gpu, rel_orc)
 
 
 def test_nvfp4_with_expcast_is_rejected(V):
