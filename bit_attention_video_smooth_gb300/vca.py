@@ -25,7 +25,7 @@ VCA_OP_GROUP, VCA_OP_PREP, VCA_OP_ATTENTION = 0, 1, 2
 # Entry points declared in include/vca.h (the ABI test checks they are exported).
 EXPORTS = ("vca_status_string", "vca_version", "vca_workspace_bytes", "vca_group", "vca_prep_quant",
            "vca_attention", "vca_expcast_codes", "vca_e4m3_encode_bits", "vca_selftest_timeout",
-           "vca_set_wait_limit_ns")
+           "vca_set_wait_limit_ns", "vca_prep_quant_noalloc")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libvca.so is not built ({LIB_PATH}); run __graft_entry__.build() -- "
@@ -44,6 +44,7 @@ _SIGS = {
     "vca_e4m3_encode_bits": (_I, [ctypes.c_uint32, _I64, _P, _P]),
     "vca_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
     "vca_set_wait_limit_ns": (None, [ctypes.c_uint64]),
+    "vca_prep_quant_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -116,6 +117,18 @@ def vca_prep_quant(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_sf, v_sca
                              _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
                              _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "vca_prep_quant")
+
+
+def vca_prep_quant_noalloc(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean,
+                           stream=None) -> None:
+    """vca_prep_quant without a workspace argument: the scratch is a buffer built
+    into the library (for callers that cannot provide device scratch memory).
+    Calls that overlap on the GPU share that buffer and must be ordered."""
+    B, H, N, d = Q.shape
+    st = _lib.vca_prep_quant_noalloc(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode,
+                                     _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf),
+                                     _ptr(v_scale), _ptr(_u16(v_mean)), _stream(stream))
+    _check(st, "vca_prep_quant_noalloc")
 
 
 def vca_attention(q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, B: int, H: int, N: int, d: int,

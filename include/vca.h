@@ -112,6 +112,29 @@ int vca_prep_quant(const uint16_t *Q, const uint16_t *K, const uint16_t *V, cons
                    void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * vca_prep_quant_noalloc -- the same computation and outputs as vca_prep_quant,
+ * for callers that cannot pass the library any scratch device memory (a host
+ * program that owns all device memory and gives an operator only its tensors,
+ * or a code path where a cudaMalloc and its possible device synchronisation are
+ * not allowed).  The paper has no counterpart to this entry point.
+ * Scratch: a buffer of VCA_NOALLOC_SCRATCH_BYTES built into the library, which
+ * every GPU that loads the library holds until the process exits.  Problems
+ * whose prep workspace (vca_workspace_bytes(VCA_OP_PREP, ...)) exceeds it return
+ * VCA_ERR_WORKSPACE and launch nothing; 16 MiB covers B*H*(N/128) up to 32,640
+ * blocks (B=1, H=40, N=70,656 needs 11.3 MB).  The first call on a device looks
+ * up the buffer's device address (make it before any stream capture).  Every
+ * call shares the one buffer: calls that overlap on the GPU race and must be
+ * ordered by the caller.  Nothing in the buffer needs clearing between calls.
+ * This entry point allocates no device memory.
+ */
+#define VCA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int vca_prep_quant_noalloc(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm,
+                           int B, int H, int N, int d, int vmode,
+                           uint8_t *q8, float *sq, uint8_t *k8, float *sk,
+                           uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean,
+                           void *stream);
+
+/*
  * vca_attention -- non-causal FP8 attention over the prepared operands (paper
  * page, "method": online softmax; ExpCast; the block means come back as one
  * outer product rowsum_b x mean_b per key block, no second pass).  For every
