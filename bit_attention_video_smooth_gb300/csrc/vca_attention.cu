@@ -7,16 +7,22 @@
 // One CTA owns a 128-row query tile of one (batch, head) and streams the key
 // blocks of that head in increasing (permuted) order.  Warp roles:
 //   warp 0     TMA producer: Q once, then K / V-residual tiles into a 3-stage ring
-//   warp 1     TMEM owner and MMA issuer (one thread): S = Q8 K8^T into one of two
-//              TMEM S buffers, O += P V8 into the TMEM O accumulator, and every
-//              16 key blocks O += [rowsum hi|lo] [mean/s_v hi|lo]^T (bf16 MMA)
+//   warp 1     TMEM owner and MMA issuer (one thread), per key block b:
+//                S[b&1] = Q8 K8_b^T                       (kind::f8f6f4, N = 128)
+//                O     += P_{b-1} V8_{b-1}                 (kind::f8f6f4, N = 128)
+//                RS[(b-1)%8] = P_{b-1} 1                   (kind::f8f6f4, N = 16)
+//              the last one writes the block's row sums of the decoded P into a
+//              rotating TMEM slot, so the softmax threads never add them up; and
+//              every 16 key blocks O += [rowsum hi|lo] [mean/s_v hi|lo]^T (bf16).
 //   warps 2-5  softmax: one thread per query row (its TMEM lane); running max,
 //              O rescale in TMEM when the max grows, P codes straight to shared
-//              memory in the 128-byte-swizzled K-major layout the PV MMA reads,
-//              per-block row sums of the decoded P, epilogue O = O s_v / l
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384).  Every wait is bounded;
-// a wait that runs out raises a CTA-wide abort, the CTA drains its copies and
-// MMAs, frees TMEM and reports VCA_ERR_TIMEOUT through the status word.
+//              memory in the 128-byte-swizzled K-major layout the MMAs read; the
+//              row sum of block b-2 is read from its TMEM slot, brought to the
+//              current max and buffered for the mean restore; epilogue
+//              O = (O s_v + the last, partial group of mean terms) / l.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), row-sum slots [384,512).
+// Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
+// drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
 #include <cuda.h>
 
 #include "vca_device.cuh"
@@ -29,8 +35,11 @@ namespace {
 constexpr int kStages = 3;
 constexpr int kThreads = 192;
 constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
+constexpr int kRsSlots = 8;                // rotating TMEM row-sum slots (16 columns each)
+constexpr int kRsCap = 32;                 // buffered row sums per thread (<= 17 in use)
 constexpr uint32_t kTileBytes = kBlk * kD; // one 128 x 128 FP8 tile (16 KB)
 constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemO = 256, kTmemRS = 384;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t kOffQ = 0;
@@ -39,8 +48,9 @@ constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
 constexpr uint32_t kOffP = kOffV + kStages * kTileBytes;
 constexpr uint32_t kOffMA = kOffP + 2 * kTileBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
-constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kMeanJ][128] buffered row sums
-constexpr uint32_t kOffSV = kOffRS + kMeanJ * kBlk * 4;     // fp32 [128] residual scales
+constexpr uint32_t kOffOnes = kOffMB + kTileBytes;          // 16 x 128 E4M3 ones (B of the row-sum MMA)
+constexpr uint32_t kOffRS = kOffOnes + 16 * 128;            // fp32 [kRsCap][128] buffered row sums
+constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residual scales
 constexpr uint32_t kOffBar = kOffSV + kBlk * 4;
 constexpr int kNumBars = 1 + 3 * kStages + 2 * 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
@@ -60,6 +70,10 @@ struct Params {
     uint64_t limit_ns;
 };
 
+// A mean-restore MMA follows PV(b) when the row sums of blocks b-17 .. b-2 are
+// all buffered (they are read two blocks late).
+__host__ __device__ constexpr bool flush_after(int b) { return b >= kMeanJ + 1 && (b % kMeanJ) == 1; }
+
 // Wait ignoring the abort flag (used only to drain work this thread issued).
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
     const uint64_t t0 = globaltimer_ns();
@@ -76,6 +90,74 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
     hi = __bfloat162float(__float2bfloat16_rn(x));
     lo = __fsub_rn(x, hi);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// packed fp32 pairs (two lanes per instruction on sm_100+)
+__device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// ExpCast for four raw scores -> four E4M3 bytes in one word (the same
+// arithmetic as expcast_rounded(): one fp32 FMA, magic-constant rounding,
+// flush below code 8, clip above 126).
+__device__ __forceinline__ uint32_t expcast4(uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3, uint64_t c8x2,
+                                             uint64_t biasx2, uint64_t magicx2) {
+    float x[4];
+    upk2(add2(fma2(pk2(s0, s1), c8x2, biasx2), magicx2), x[0], x[1]);
+    upk2(add2(fma2(pk2(s2, s3), c8x2, biasx2), magicx2), x[2], x[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[e] = (x[e] >= kMagic + 8.0f) ? x[e] : kMagic;
+        x[e] = fminf(x[e], kMagic + 126.0f);
+    }
+    return __byte_perm(__byte_perm(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x0040),
+                       __byte_perm(__float_as_uint(x[2]), __float_as_uint(x[3]), 0x0040), 0x5410);
+}
+
+// exp2 then E4M3 for four raw scores: p = 2^(fma(S, c, -m)).
+__device__ __forceinline__ uint32_t expconv4(uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3, uint64_t cx2,
+                                             uint64_t negmx2) {
+    float a[4];
+    upk2(fma2(pk2(s0, s1), cx2, negmx2), a[0], a[1]);
+    upk2(fma2(pk2(s2, s3), cx2, negmx2), a[2], a[3]);
+    return e4m3x2(ex2_approx(a[0]), ex2_approx(a[1])) | (e4m3x2(ex2_approx(a[2]), ex2_approx(a[3])) << 16);
+}
+
+__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Named barrier over the four softmax warps that also ANDs a flag across them.
+__device__ __forceinline__ bool softmax_all(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v))
+        : "memory");
+    return r != 0;
 }
 
 template <bool kExpcast>
@@ -126,7 +208,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (warp >= 2) sSV[threadIdx.x - 64] = p.v_scale[static_cast<int64_t>(bh) * kD + (threadIdx.x - 64)];
+    if (warp >= 2) {
+        const int t = threadIdx.x - 64;
+        sSV[t] = p.v_scale[static_cast<int64_t>(bh) * kD + t];
+        // the ones tile: 16 rows x 128 bytes of E4M3 1.0 (0x38)
+        *reinterpret_cast<uint4 *>(smem + kOffOnes + 16 * t) = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        fence_proxy_async_smem();
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -163,12 +251,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_f8 = make_idesc(128, 128, 0, 0);
+            constexpr uint32_t idesc_rs = make_idesc(128, 16, 0, 0);
             constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
             const uint32_t sbase = smem_u32(smem);
             const uint64_t dq = sdesc_k_sw128(sbase + kOffQ);
             const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
             const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
-            const uint32_t tO = tmem + 256;
+            const uint64_t dones = sdesc_k_sw128(sbase + kOffOnes);
+            const uint32_t tO = tmem + kTmemO;
             bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
             for (int b = 0; ok && b <= nb; ++b) {
                 if (b < nb) {
@@ -192,7 +282,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int kk = 0; kk < kBlk / 32; ++kk)
                         mma_f8f6f4(tO, dp + 2 * kk, dv + 2 * kk, idesc_f8, (j > 0 || kk > 0) ? 1u : 0u);
-                    if ((j % kMeanJ) == kMeanJ - 1 || j == nb - 1) {
+                    const uint32_t trs = tmem + kTmemRS + 16 * (j % kRsSlots);
+#pragma unroll
+                    for (int kk = 0; kk < kBlk / 32; ++kk)
+                        mma_f8f6f4(trs, dp + 2 * kk, dones + 2 * kk, idesc_rs, kk > 0 ? 1u : 0u);
+                    if (flush_after(j)) {
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
                     }
@@ -208,36 +302,58 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int quarter = warp & 3;
         const int row = quarter * 32 + lane;                       // query row in the tile == TMEM lane
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tO = tmem + lane_base + 256;
+        const uint32_t tO = tmem + lane_base + kTmemO;
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
+        const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
         unsigned char *sP = smem + kOffP;
         unsigned char *sMA = smem + kOffMA;
         unsigned char *sMB = smem + kOffMB;
-        float m = __int_as_float(0xff800000);   // -inf
+        const float kNegInf = __int_as_float(0xff800000);
+        float m = kNegInf, mh1 = kNegInf, mh2 = kNegInf;   // running max; the max of blocks b-1, b-2
         float l = 0.0f;
         int rs_cnt = 0;
         bool ok = true;
+        float sk_next = skh[0];
         for (int b = 0; b < nb; ++b) {
             const int sb = b & 1;
+            const float sk_b = sk_next;
+            if (b + 1 < nb) sk_next = skh[b + 1];
             ok = __all_sync(0xffffffffu, mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns));
             if (!ok) break;
+            // PV(b-2) and its row sums are done (also frees P buffer sb)
+            if (b >= 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns));
+                if (!ok) break;
+            }
             tc_fence_after();
             uint32_t S[128];
+            uint32_t rs_raw = 0;
             const uint32_t tS = tmem + lane_base + sb * 128;
             VCA_TMEM_LD32(tS + 0, (S + 0));
             VCA_TMEM_LD32(tS + 32, (S + 32));
             VCA_TMEM_LD32(tS + 64, (S + 64));
             VCA_TMEM_LD32(tS + 96, (S + 96));
+            if (b >= 2) {
+                const uint32_t trs = tmem + lane_base + kTmemRS + 16 * ((b - 2) % kRsSlots);
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(trs));
+            }
             tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(B.s_free + sb);
 
-            const float c = __fmul_rn(__fmul_rn(sqv, skh[b]), p.scale_log2);
-            float smax = __uint_as_float(S[0]);
+            const float c = __fmul_rn(__fmul_rn(sqv, sk_b), p.scale_log2);
+            float a0 = __uint_as_float(S[0]), a1 = __uint_as_float(S[1]);
+            float a2 = __uint_as_float(S[2]), a3 = __uint_as_float(S[3]);
 #pragma unroll
-            for (int j = 1; j < 128; ++j) smax = fmaxf(smax, __uint_as_float(S[j]));
+            for (int j = 4; j < 128; j += 8) {
+                a0 = max3(a0, __uint_as_float(S[j + 0]), __uint_as_float(S[j + 1]));
+                a1 = max3(a1, __uint_as_float(S[j + 2]), __uint_as_float(S[j + 3]));
+                a2 = max3(a2, __uint_as_float(S[j + 4]), __uint_as_float(S[j + 5]));
+                a3 = max3(a3, __uint_as_float(S[j + 6]), __uint_as_float(S[j + 7]));
+            }
+            const float smax = fmaxf(max3(a0, a1, a2), a3);
             const float m_new = fmaxf(m, __fmul_rn(smax, c));
             float alpha = 1.0f;
             if (m_new > m && b > 0) alpha = ex2_approx(__fsub_rn(m, m_new));
@@ -245,66 +361,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
             if (alpha != 1.0f) {
                 l = __fmul_rn(l, alpha);
+#pragma unroll 1
                 for (int i = 0; i < rs_cnt; ++i) sRS[i * kBlk + row] = __fmul_rn(sRS[i * kBlk + row], alpha);
             }
-
-            // P buffer sb was last read by PV(b-2)
             if (b >= 2) {
-                ok = __all_sync(0xffffffffu,
-                                mbar_wait(B.pv_done + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns));
-                if (!ok) break;
+                // row sum of block b-2, taken against that block's max: bring it to m
+                float rs = __uint_as_float(rs_raw);
+                if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
+                l = __fadd_rn(l, rs);
+                sRS[rs_cnt * kBlk + row] = rs;
+                ++rs_cnt;
             }
-            float rowsum = 0.0f;
+
             unsigned char *prow = sP + sb * kTileBytes;
             if constexpr (kExpcast) {
                 const float c8 = __fmul_rn(8.0f, c);
                 const float bias = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m));
+                const uint64_t c8x2 = pk2(__float_as_uint(c8), __float_as_uint(c8));
+                const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
+                const uint64_t mx2 = pk2(__float_as_uint(kMagic), __float_as_uint(kMagic));
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float x[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            x[e] = expcast_rounded(__uint_as_float(S[ch * 16 + q * 4 + e]), c8, bias);
-                            rowsum = __fadd_rn(rowsum, expcast_value(x[e]));
-                        }
-                        w[q] = __byte_perm(__byte_perm(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x0040),
-                                           __byte_perm(__float_as_uint(x[2]), __float_as_uint(x[3]), 0x0040),
-                                           0x5410);
-                    }
-                    *reinterpret_cast<uint4 *>(prow + sw128_offset(row, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    const uint32_t *s = S + ch * 16;
+                    const uint32_t w0 = expcast4(s[0], s[1], s[2], s[3], c8x2, bx2, mx2);
+                    const uint32_t w1 = expcast4(s[4], s[5], s[6], s[7], c8x2, bx2, mx2);
+                    const uint32_t w2 = expcast4(s[8], s[9], s[10], s[11], c8x2, bx2, mx2);
+                    const uint32_t w3 = expcast4(s[12], s[13], s[14], s[15], c8x2, bx2, mx2);
+                    *reinterpret_cast<uint4 *>(prow + sw128_offset(row, ch)) = make_uint4(w0, w1, w2, w3);
                 }
             } else {
                 const float negm = -m;
+                const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
+                const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch) {
-                    uint32_t w[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        float pr[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e)
-                            pr[e] = ex2_approx(__fmaf_rn(__uint_as_float(S[ch * 16 + q * 4 + e]), c, negm));
-                        const uint32_t lo = e4m3x2(pr[0], pr[1]), hi = e4m3x2(pr[2], pr[3]);
-                        w[q] = lo | (hi << 16);
-                        rowsum = __fadd_rn(rowsum, e4m3_to_f32(lo & 0xFF));
-                        rowsum = __fadd_rn(rowsum, e4m3_to_f32(lo >> 8));
-                        rowsum = __fadd_rn(rowsum, e4m3_to_f32(hi & 0xFF));
-                        rowsum = __fadd_rn(rowsum, e4m3_to_f32(hi >> 8));
-                    }
-                    *reinterpret_cast<uint4 *>(prow + sw128_offset(row, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+                    const uint32_t *s = S + ch * 16;
+                    const uint32_t w0 = expconv4(s[0], s[1], s[2], s[3], cx2, nx2);
+                    const uint32_t w1 = expconv4(s[4], s[5], s[6], s[7], cx2, nx2);
+                    const uint32_t w2 = expconv4(s[8], s[9], s[10], s[11], cx2, nx2);
+                    const uint32_t w3 = expconv4(s[12], s[13], s[14], s[15], cx2, nx2);
+                    *reinterpret_cast<uint4 *>(prow + sw128_offset(row, ch)) = make_uint4(w0, w1, w2, w3);
                 }
             }
 
-            // rescale the O accumulator after PV(b-1) (and its mean MMA) finished
+            // rescale the O accumulator after PV(b-1) (and any mean MMA after it) finished
             if (rescale) {
                 const int jb = b - 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + (jb & 1), (jb >> 1) & 1, abort_flag, p.limit_ns));
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int i = 0; i < 4; ++i) {
                     uint32_t o[32];
                     VCA_TMEM_LD32(tO + 32 * i, o);
@@ -316,25 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_st_wait();
             }
 
-            sRS[rs_cnt * kBlk + row] = rowsum;
-            ++rs_cnt;
-            l = __fadd_rn(l, rowsum);
-            if ((b % kMeanJ) == kMeanJ - 1 || b == nb - 1) {
-                // A row (this query row): [rs hi | rs lo | rs hi | rs lo], 16 blocks each
+            if (flush_after(b)) {
+                // row sums of blocks b0 .. b0+15 (all at the current max):
+                // A row (this query row): [rs hi | rs lo | rs hi | rs lo]
                 // B row (channel `row`):  [mu hi | mu hi | mu lo | mu lo], mu = mean / s_v
-                const int b0 = b - (rs_cnt - 1);
+                const int b0 = b - kMeanJ - 1;
                 const float inv_sv = 1.0f / sSV[row];
                 float rh[kMeanJ], rl[kMeanJ], mh[kMeanJ], ml[kMeanJ];
 #pragma unroll
                 for (int i = 0; i < kMeanJ; ++i) {
-                    float r = 0.0f, u = 0.0f;
-                    if (i < rs_cnt) {
-                        r = sRS[i * kBlk + row];
-                        u = __fmul_rn(bf16_bits_to_f32(p.v_mean[(static_cast<int64_t>(bh) * nb + b0 + i) * kD + row]),
-                                      inv_sv);
-                    }
-                    split_bf16(r, rh[i], rl[i]);
-                    split_bf16(u, mh[i], ml[i]);
+                    split_bf16(sRS[i * kBlk + row], rh[i], rl[i]);
+                    split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), mh[i], ml[i]);
                 }
 #pragma unroll
                 for (int ck = 0; ck < 8; ++ck) {
@@ -359,28 +457,70 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(B.p_full + sb);
+            mh2 = mh1;
+            mh1 = m;
         }
         // ------------------------------------------------------------ epilogue
         if (ok) {
             const int jb = nb - 1;
             ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + (jb & 1), (jb >> 1) & 1, abort_flag, p.limit_ns));
         }
+        // every softmax warp arrives here, whether it finished or gave up; the
+        // epilogue (and its named barrier) runs only if all four finished
+        ok = softmax_all(ok);
         if (ok) {
             tc_fence_after();
+            // the last two blocks' row sums
+            uint32_t r2 = 0, r1 = 0;
+            const uint32_t tr = tmem + lane_base + kTmemRS;
+            if (nb >= 2)
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                             : "=r"(r2) : "r"(tr + 16 * ((nb - 2) % kRsSlots)));
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                         : "=r"(r1) : "r"(tr + 16 * ((nb - 1) % kRsSlots)));
+            tmem_ld_wait();
+            if (nb >= 2) {
+                float rs = __uint_as_float(r2);
+                if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
+                l = __fadd_rn(l, rs);
+                sRS[rs_cnt * kBlk + row] = rs;
+                ++rs_cnt;
+            }
+            {
+                const float rs = __uint_as_float(r1);   // taken against m itself
+                l = __fadd_rn(l, rs);
+                sRS[rs_cnt * kBlk + row] = rs;
+                ++rs_cnt;
+            }
+            // the blocks since the last mean MMA: stage their means (fp32) in the
+            // mean-B buffer, whose last reader (the final mean MMA) has finished
+            const int tail0 = nb - rs_cnt;
+            float *sMu = reinterpret_cast<float *>(sMB);
+            softmax_bar();
+            for (int i = threadIdx.x - 64; i < rs_cnt * kD; i += 128)
+                sMu[i] = bf16_bits_to_f32(vmh[(tail0 + i / kD) * kD + (i % kD)]);
+            softmax_bar();
             const float inv_l = 1.0f / l;
             uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD;
-#pragma unroll
+#pragma unroll 1
             for (int i = 0; i < 4; ++i) {
                 uint32_t o[32];
                 VCA_TMEM_LD32(tO + 32 * i, o);
                 tmem_ld_wait();
+                float acc[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) acc[e] = __fmul_rn(__uint_as_float(o[e]), sSV[32 * i + e]);
+#pragma unroll 1
+                for (int t = 0; t < rs_cnt; ++t) {
+                    const float r = sRS[t * kBlk + row];
+                    const float *mu = sMu + t * kD + 32 * i;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) acc[e] = __fmaf_rn(r, mu[e], acc[e]);
+                }
                 uint32_t w[16];
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int c0 = 32 * i + 2 * e;
-                    w[e] = pack_bf16x2(__fmul_rn(__fmul_rn(__uint_as_float(o[2 * e]), sSV[c0]), inv_l),
-                                       __fmul_rn(__fmul_rn(__uint_as_float(o[2 * e + 1]), sSV[c0 + 1]), inv_l));
-                }
+                for (int e = 0; e < 16; ++e)
+                    w[e] = pack_bf16x2(__fmul_rn(acc[2 * e], inv_l), __fmul_rn(acc[2 * e + 1], inv_l));
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
                     reinterpret_cast<uint4 *>(orow + 32 * i)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
