@@ -70,7 +70,7 @@ def _load():
                 "orc_kmeans_sse": (ctypes.c_double, [P, i32, i32, P, P]),
                 "orc_prep": (i32, [P, P, P, P, i32, i32, i32, i32,
                                    P, P, P, P, P, P, P, P]),
-                "orc_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, f32, i32, i32,
+                "orc_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, f32, f32, i32, i32,
                                         P, i32, P, P]),
                 "orc_attention_exact": (i32, [P, P, P, i32, i32, i32, f32, P, i32, P]),
             }
@@ -241,13 +241,18 @@ def prep(Q, K, V, perm, vmode: int = V_E4M3) -> dict:
 # ---------------------------------------------------------------------------
 # Attention (paper page "method": online softmax, ExpCast, mean restore)
 # ---------------------------------------------------------------------------
+TAU = 8.0   # lazy-rescale threshold of the kernel (log2 units)
+
+
 def attention(prepped: dict, mode: int, softmax_scale: float = 0.0, rows=None,
-              return_l: bool = False):
+              return_l: bool = False, tau: float = TAU):
     """Schedule-emulating attention on prepared operands.
 
     mode: P_EXPCAST, P_EXP, P_NVFP4 or P_EXACT (P unquantised; a pin mode).
     The residual format (E4M3 or NVFP4) follows ``prepped`` (NVFP4 when it
-    holds ``v_sf``).  rows: optional int array of query rows computed for every
+    holds ``v_sf``).  tau: the reference max moves to a block's max only when
+    that exceeds it by more than tau (FlashAttention-4's lazy rescale; 0 gives
+    the plain running max).  rows: optional int array of query rows computed for every
     (b,h).  Returns bf16 O [BH, nrows, d] (uint16), optionally l.
     """
     lib = _load()
@@ -259,7 +264,7 @@ def attention(prepped: dict, mode: int, softmax_scale: float = 0.0, rows=None,
     l = np.empty((BH, nrows), np.float64) if return_l else None
     rc = lib.orc_attention(_p(q8), _p(prepped["sq"]), _p(prepped["k8"]), _p(prepped["sk"]),
                            _p(prepped["v_res"]), _p(prepped.get("v_sf")), _p(prepped["v_scale"]),
-                           _p(prepped["v_mean"]), BH, N, d, float(softmax_scale), mode,
+                           _p(prepped["v_mean"]), BH, N, d, float(softmax_scale), float(tau), mode,
                            V_E4M3 if prepped.get("v_sf") is None else V_NVFP4,
                            _p(r), nrows, _p(O), _p(l))
     if rc:

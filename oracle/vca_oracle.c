@@ -21,9 +21,12 @@
  *   R3  `iters` rounds of (assign, update); labels are those of the last assign.
  *   R4  ExpCast code = rne(8 log2 p + 56 + beta), beta = -0.35, one fp32 FMA.
  *   R5  codes below the E4M3 normal range (< 8) flush to 0; codes > 126 -> 126.
- *   R6  P is coded against the running max over key blocks 0..b (inclusive),
- *       blocks visited in increasing (permuted) order; alpha = 2^(m_old-m_new)
- *       rescales the accumulators whenever the max grows.
+ *   R6  P is coded against a reference max m taken from the key blocks 0..b
+ *       visited in increasing (permuted) order.  The pages' kernel is built on
+ *       FlashAttention-4, which rescales lazily: m moves to the block max only
+ *       when that max exceeds m + tau (log2 units; tau = 8 in the kernel,
+ *       tau = 0 is the plain running max), and alpha = 2^(m_old - m_new) then
+ *       rescales the accumulators.  P values stay below 2^tau.
  *   R7  one E4M3 residual scale per (batch, head, channel) over the sequence.
  *   R8  Q/K: one absmax/448 scale per (batch, head, 128-token block).
  *   R9  NVFP4 residual: 16 consecutive tokens of one channel share an E4M3
@@ -403,6 +406,7 @@ int orc_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int3
 /* ------------------------------------------------------------------------- */
 /* Attention with V-Smooth restore and ExpCast, emulating the kernel's        */
 /* online-softmax schedule (R6): key blocks in increasing permuted order,      */
+/* reference max updated lazily (threshold tau),                               */
 /* running max, alpha rescale, per-block row sums of the decoded P (R11) and   */
 /* the mean restored as one outer product per block (paper page, "method":    */
 /* the block means come back through the row sums online softmax already      */
@@ -415,7 +419,7 @@ int orc_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int3
 /* ------------------------------------------------------------------------- */
 int orc_attention(const uint8_t *q8, const float *sq, const uint8_t *k8, const float *sk,
                   const uint8_t *v_res, const uint8_t *v_sf, const float *v_scale, const uint16_t *v_mean,
-                  int BH, int N, int d, float softmax_scale, int mode, int vmode,
+                  int BH, int N, int d, float softmax_scale, float tau, int mode, int vmode,
                   const int32_t *rows, int nrows, uint16_t *O, double *l_out)
 {
     if (N % BLK != 0 || d <= 0) return 1;
@@ -467,13 +471,15 @@ int orc_attention(const uint8_t *q8, const float *sq, const uint8_t *k8, const f
                     float s = S[j] * c;
                     if (s > bmax) bmax = s;
                 }
-                float m_new = (bmax > m) ? bmax : m;
-                if (m_new > m && m != -INFINITY) {
-                    double alpha = exp2((double)m - (double)m_new);
-                    for (int x = 0; x < d; x++) { acc[x] *= alpha; mac[x] *= alpha; }
-                    l *= alpha;
+                /* lazy update of the reference max (R6): fp32 m + tau */
+                if (bmax > m + tau) {
+                    if (m != -INFINITY) {
+                        double alpha = exp2((double)m - (double)bmax);
+                        for (int x = 0; x < d; x++) { acc[x] *= alpha; mac[x] *= alpha; }
+                        l *= alpha;
+                    }
+                    m = bmax;
                 }
-                m = m_new;
                 double rowsum = 0.0;
                 if (mode == ORC_P_NVFP4) {
                     for (int g = 0; g < BLK; g += 16) {

@@ -82,8 +82,8 @@ def test_exact_attention_matches_sdpa_and_is_permutation_invariant(orc):
     np.testing.assert_allclose(orc.attention_exact(q, k, v, rows=rows), O[:, rows], rtol=0, atol=0)
 
 
-def _two_block_case(orc):
-    """One (b,h), N = 256, d = 128: query row 0 is e4m3 1.0 on channel 0; key j
+def _two_block_case(orc, third=False):
+    """One (b,h), N = 256 (384 with `third`), d = 128: query row 0 is e4m3 1.0 on channel 0; key j
     carries a_j on channel 0, so S_raw = a_j; sq = sk = 1 and the softmax scale
     is fp32(ln 2), making c = 1 and s = S_raw.
 
@@ -92,20 +92,24 @@ def _two_block_case(orc):
     V: residual scale 1; mean 0.5 in block 0, -0.25 in block 1; residual codes
     2.0 at (key 1, ch 0), -1.0 at (key 0, ch 1), 1.0 at (key 129, ch 1).
     """
-    N, d = 256, 128
-    code = {v: int(orc.e4m3_encode(np.array([v], np.float32))[0]) for v in (1.0, 0.3125, 4.5, 2.0, -1.0)}
+    N, d = (384 if third else 256), 128
+    code = {v: int(orc.e4m3_encode(np.array([v], np.float32))[0]) for v in (1.0, 0.3125, 4.5, 2.0, -1.0, 12.0)}
     q8 = np.zeros((1, N, d), np.uint8)
     q8[0, :, 0] = code[1.0]
     k8 = np.zeros((1, N, d), np.uint8)
     k8[0, 0, 0], k8[0, 1, 0], k8[0, 128, 0], k8[0, 129, 0] = code[1.0], code[0.3125], code[4.5], code[2.0]
-    v_res = np.zeros((1, 2, d, 128), np.uint8)
+    nb = N // 128
+    v_res = np.zeros((1, nb, d, 128), np.uint8)
     v_res[0, 0, 0, 1] = code[2.0]
     v_res[0, 0, 1, 0] = code[-1.0]
     v_res[0, 1, 1, 1] = code[1.0]
-    v_mean = np.zeros((1, 2, d), np.uint16)
+    v_mean = np.zeros((1, nb, d), np.uint16)
     v_mean[0, 0, :] = orc.bf16_round(0.5)
     v_mean[0, 1, :] = orc.bf16_round(-0.25)
-    return {"q8": q8, "sq": np.ones((1, 2), np.float32), "k8": k8, "sk": np.ones((1, 2), np.float32),
+    if third:                      # block 2: a = 12 at key 256, mean 1.0
+        k8[0, 256, 0] = code[12.0]
+        v_mean[0, 2, :] = orc.bf16_round(1.0)
+    return {"q8": q8, "sq": np.ones((1, nb), np.float32), "k8": k8, "sk": np.ones((1, nb), np.float32),
             "v_res": v_res, "v_sf": None, "v_scale": np.ones((1, d), np.float32), "v_mean": v_mean}
 
 
@@ -121,7 +125,8 @@ def test_running_max_schedule_worked_example(orc):
     ch0 = (a * (0.625 * 2.0 + 64.625 * 0.5) + 7.09375 * -0.25) / l
     ch1 = (a * (1.0 * -1.0 + 64.625 * 0.5) + (0.1875 * 1.0 + 7.09375 * -0.25)) / l
     rest = (a * 64.625 * 0.5 + 7.09375 * -0.25) / l
-    O, lo = orc.attention(p, orc.P_EXPCAST, softmax_scale=LN2_F32, rows=np.array([0], np.int32), return_l=True)
+    O, lo = orc.attention(p, orc.P_EXPCAST, softmax_scale=LN2_F32, rows=np.array([0], np.int32), return_l=True,
+                          tau=0.0)
     got = _f32(O[0, 0])
     assert lo[0, 0] == pytest.approx(l, rel=1e-15)
     assert got[0] == np.float32(_f32(orc.bf16_round(ch0)))
@@ -135,9 +140,43 @@ def test_running_max_schedule_worked_example(orc):
     r1 = 1.0 + 0.171875 + 126 * 0.04296875
     l2 = 64.625 * a + r1
     rest2 = (a * 64.625 * 0.5 + r1 * -0.25) / l2
-    O2, lo2 = orc.attention(p, orc.P_EXP, softmax_scale=LN2_F32, rows=np.array([0], np.int32), return_l=True)
+    O2, lo2 = orc.attention(p, orc.P_EXP, softmax_scale=LN2_F32, rows=np.array([0], np.int32), return_l=True,
+                            tau=0.0)
     assert lo2[0, 0] == pytest.approx(l2, rel=1e-15)
     assert np.all(_f32(O2[0, 0])[2:] == np.float32(_f32(orc.bf16_round(rest2))))
+
+
+def test_lazy_rescale_worked_example(orc):
+    """tau = 8 (FlashAttention-4's lazy rescale): the reference max moves only
+    when a block's max exceeds it by more than 8 (log2 units)."""
+    row = np.array([0], np.int32)
+    p = _two_block_case(orc, third=True)
+    # block 0: m = 1, codes as in the tau = 0 example, rowsum0 = 64.625
+    # block 1: 4.5 <= 1 + 8, m stays 1: key128 t=83.65 -> 84 (12.0); key129
+    #          t=63.65 -> 64 (2.0); zeros t=47.65 -> 48 (0.5) x126  rowsum1 = 77
+    # block 2: 12 > 1 + 8: alpha = 2^-11, m = 12; key256 -> 56 (1.0); zeros
+    #          t=-40.35 -> flushed                                   rowsum2 = 1
+    a = 2.0 ** -11
+    l = (64.625 + 77.0) * a + 1.0
+    ch0 = ((0.625 * 2.0 + 64.625 * 0.5 + 77.0 * -0.25) * a + 1.0) / l
+    ch1 = ((-1.0 + 64.625 * 0.5 + 2.0 * 1.0 + 77.0 * -0.25) * a + 1.0) / l
+    rest = ((64.625 * 0.5 + 77.0 * -0.25) * a + 1.0) / l
+    O, lo = orc.attention(p, orc.P_EXPCAST, softmax_scale=LN2_F32, rows=row, return_l=True, tau=8.0)
+    got = _f32(O[0, 0])
+    assert lo[0, 0] == pytest.approx(l, rel=1e-15)
+    assert got[0] == np.float32(_f32(orc.bf16_round(ch0)))
+    assert got[1] == np.float32(_f32(orc.bf16_round(ch1)))
+    assert np.all(got[2:] == np.float32(_f32(orc.bf16_round(rest))))
+    # two blocks only, exp path: block 1 against m = 1: 2^3.5 = 11.31 -> 11 (83);
+    # 2^1 -> 2 (64); 2^-1 -> 0.5                                      rowsum1 = 76
+    p2 = _two_block_case(orc)
+    O2, lo2 = orc.attention(p2, orc.P_EXP, softmax_scale=LN2_F32, rows=row, return_l=True, tau=8.0)
+    assert lo2[0, 0] == pytest.approx(64.625 + 76.0, rel=1e-15)
+    rest2 = (64.625 * 0.5 + 76.0 * -0.25) / (64.625 + 76.0)
+    assert np.all(_f32(O2[0, 0])[2:] == np.float32(_f32(orc.bf16_round(rest2))))
+    # with tau = 0 the same two blocks rescale at block 1 (the earlier example)
+    _, lo3 = orc.attention(p2, orc.P_EXP, softmax_scale=LN2_F32, rows=row, return_l=True, tau=0.0)
+    assert lo3[0, 0] != pytest.approx(lo2[0, 0])
 
 
 @pytest.mark.parametrize("mode", [0, 1, 2, 3])
