@@ -14,12 +14,15 @@
 //              the last one writes the block's row sums of the decoded P into a
 //              rotating TMEM slot, so the softmax threads never add them up; and
 //              every 16 key blocks O += [rowsum hi|lo] [mean/s_v hi|lo]^T (bf16).
-//   warps 2-5  softmax: one thread per query row (its TMEM lane); running max,
-//              O rescale in TMEM when the max grows, P codes straight to shared
-//              memory in the 128-byte-swizzled K-major layout the MMAs read; the
-//              row sum of block b-2 is read from its TMEM slot, brought to the
-//              current max and buffered for the mean restore; epilogue
-//              O = (O s_v + the last, partial group of mean terms) / l.
+//   warps 2-9  softmax: two threads per query row -- the warps w and w+4 share
+//              a TMEM lane quarter and take the S columns 0-63 and 64-127; the
+//              pair exchanges its half-row maxima through shared memory at a
+//              64-thread named barrier.  Running max, O rescale in TMEM when the
+//              max grows, P codes straight to shared memory in the
+//              128-byte-swizzled K-major layout the MMAs read; the row sum of
+//              block b-2 is read from its TMEM slot, brought to the current max
+//              and buffered for the mean restore; epilogue O = (O s_v + the
+//              last, partial group of mean terms) / l.
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), row-sum slots [384,512).
 // Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
 // drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
@@ -33,10 +36,11 @@ namespace vca {
 namespace {
 
 constexpr int kStages = 3;
-constexpr int kThreads = 192;
+constexpr int kSoftmaxWarps = 8;
+constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
 constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
 constexpr int kRsSlots = 8;                // rotating TMEM row-sum slots (16 columns each)
-constexpr int kRsCap = 32;                 // buffered row sums per thread (<= 17 in use)
+constexpr int kRsCap = 32;                 // buffered row sums per row (<= 17 in use)
 constexpr uint32_t kTileBytes = kBlk * kD; // one 128 x 128 FP8 tile (16 KB)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemO = 256, kTmemRS = 384;
@@ -51,7 +55,9 @@ constexpr uint32_t kOffMB = kOffMA + kTileBytes;
 constexpr uint32_t kOffOnes = kOffMB + kTileBytes;          // 16 x 128 E4M3 ones (B of the row-sum MMA)
 constexpr uint32_t kOffRS = kOffOnes + 16 * 128;            // fp32 [kRsCap][128] buffered row sums
 constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residual scales
-constexpr uint32_t kOffBar = kOffSV + kBlk * 4;
+constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][2][128] half-row maxima
+constexpr uint32_t kOffL = kOffPM + 4 * kBlk * 4;           // fp32 [128] final row sums
+constexpr uint32_t kOffBar = kOffL + kBlk * 4;
 constexpr int kNumBars = 1 + 3 * kStages + 2 * 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
@@ -98,66 +104,83 @@ __device__ __forceinline__ float max3(float a, float b, float c) {
     return d;
 }
 
-// packed fp32 pairs (two lanes per instruction on sm_100+)
-__device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
-    uint64_t d;
-    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
-    return d;
-}
-__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
-    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-
-// ExpCast for four raw scores -> four E4M3 bytes in one word (the same
-// arithmetic as expcast_rounded(): one fp32 FMA, magic-constant rounding,
-// flush below code 8, clip above 126).
-__device__ __forceinline__ uint32_t expcast4(uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3, uint64_t c8x2,
-                                             uint64_t biasx2, uint64_t magicx2) {
-    float x[4];
-    upk2(add2(fma2(pk2(s0, s1), c8x2, biasx2), magicx2), x[0], x[1]);
-    upk2(add2(fma2(pk2(s2, s3), c8x2, biasx2), magicx2), x[2], x[3]);
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-        x[e] = (x[e] >= kMagic + 8.0f) ? x[e] : kMagic;
-        x[e] = fminf(x[e], kMagic + 126.0f);
-    }
-    return __byte_perm(__byte_perm(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x0040),
-                       __byte_perm(__float_as_uint(x[2]), __float_as_uint(x[3]), 0x0040), 0x5410);
-}
-
 // exp2 then E4M3 for four raw scores: p = 2^(fma(S, c, -m)).
-__device__ __forceinline__ uint32_t expconv4(uint32_t s0, uint32_t s1, uint32_t s2, uint32_t s3, uint64_t cx2,
-                                             uint64_t negmx2) {
+__device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_t cx2, uint64_t negmx2) {
     float a[4];
-    upk2(fma2(pk2(s0, s1), cx2, negmx2), a[0], a[1]);
-    upk2(fma2(pk2(s2, s3), cx2, negmx2), a[2], a[3]);
+    upk2(fma2(s01, cx2, negmx2), a[0], a[1]);
+    upk2(fma2(s23, cx2, negmx2), a[2], a[3]);
     return e4m3x2(ex2_approx(a[0]), ex2_approx(a[1])) | (e4m3x2(ex2_approx(a[2]), ex2_approx(a[3])) << 16);
 }
 
-__device__ __forceinline__ void softmax_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// Named barrier over the four softmax warps that also ANDs a flag across them.
-__device__ __forceinline__ bool softmax_all(bool v) {
+// Named barrier that also ANDs a flag over its `count` threads.
+__device__ __forceinline__ bool bar_and(bool v, uint32_t id, uint32_t count) {
     uint32_t r;
     asm volatile(
         "{\n\t.reg .pred p, q;\n\t"
         "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, 1, 128, p;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
         "selp.u32 %0, 1, 0, q;\n\t}\n"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(v))
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
         : "memory");
     return r != 0;
+}
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+constexpr uint32_t kBarSoftmax = 1;   // all softmax warps (256 threads)
+constexpr uint32_t kBarPair0 = 2;     // + quarter: the two warps of one TMEM lane quarter (64 threads)
+
+constexpr float kLazyTau = 8.0f;      // log2 units: the reference max moves by more than 2^8 only
+
+// P codes of this thread's half row (64 keys) against the reference max m,
+// written as four 16-byte chunks of the 128-byte-swizzled P tile.
+template <bool kExpcast>
+__device__ __forceinline__ void write_codes(const uint32_t (&S)[64], float c, float m, unsigned char *prow, int row,
+                                            int half) {
+    if constexpr (kExpcast) {
+        const float c8 = __fmul_rn(8.0f, c);
+        const float bias = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m));
+        const uint64_t c8x2 = pk2(__float_as_uint(c8), __float_as_uint(c8));
+        const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
+        if (__all_sync(0xffffffffu, fabsf(m) < kExpcastFastMax)) {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = ch * 16 + 4 * q;
+                    w[q] = expcast4<false>(pk2(S[j], S[j + 1]), pk2(S[j + 2], S[j + 3]), c8x2, c8x2, bx2, bx2);
+                }
+                *reinterpret_cast<uint4 *>(prow + sw128_offset(row, 4 * half + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        } else {
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t w[4];
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int j = ch * 16 + 4 * q;
+                    w[q] = expcast4<true>(pk2(S[j], S[j + 1]), pk2(S[j + 2], S[j + 3]), c8x2, c8x2, bx2, bx2);
+                }
+                *reinterpret_cast<uint4 *>(prow + sw128_offset(row, 4 * half + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+            }
+        }
+    } else {
+        const float negm = -m;
+        const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
+        const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int j = ch * 16 + 4 * q;
+                w[q] = expconv4(pk2(S[j], S[j + 1]), pk2(S[j + 2], S[j + 3]), cx2, nx2);
+            }
+            *reinterpret_cast<uint4 *>(prow + sw128_offset(row, 4 * half + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    }
 }
 
 template <bool kExpcast>
@@ -182,6 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int *abort_flag = reinterpret_cast<int *>(smem + kOffMisc + 4);
     float *sRS = reinterpret_cast<float *>(smem + kOffRS);
     float *sSV = reinterpret_cast<float *>(smem + kOffSV);
+    float *sPM = reinterpret_cast<float *>(smem + kOffPM);
+    float *sL = reinterpret_cast<float *>(smem + kOffL);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qtile = blockIdx.x, bh = blockIdx.y;
@@ -196,8 +221,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(B.s_full + i, 1);
-            mbar_init(B.s_free + i, 4);
-            mbar_init(B.p_full + i, 4);
+            mbar_init(B.s_free + i, kSoftmaxWarps);
+            mbar_init(B.p_full + i, kSoftmaxWarps);
             mbar_init(B.pv_done + i, 1);
         }
         mbar_init(B.drain, 1);
@@ -208,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
-    if (warp >= 2) {
+    if (warp >= 2 && warp < 6) {
         const int t = threadIdx.x - 64;
         sSV[t] = p.v_scale[static_cast<int64_t>(bh) * kD + t];
         // the ones tile: 16 rows x 128 bytes of E4M3 1.0 (0x38)
@@ -299,10 +324,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int quarter = warp & 3;
+        const int quarter = warp & 3;                              // TMEM lane quarter
+        const int half = (warp - 2) >> 2;                          // S columns 64*half .. 64*half+63
         const int row = quarter * 32 + lane;                       // query row in the tile == TMEM lane
+        const uint32_t pair_bar = kBarPair0 + quarter;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t tO = tmem + lane_base + kTmemO;
+        const uint32_t col0 = 64u * half;
+        const uint32_t tO = tmem + lane_base + kTmemO + col0;
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
         const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
@@ -311,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         unsigned char *sMB = smem + kOffMB;
         const float kNegInf = __int_as_float(0xff800000);
         float m = kNegInf, mh1 = kNegInf, mh2 = kNegInf;   // running max; the max of blocks b-1, b-2
-        float l = 0.0f;
+        float l = 0.0f;                                    // kept by the half-0 thread of the row
         int rs_cnt = 0;
         bool ok = true;
         float sk_next = skh[0];
@@ -319,144 +347,126 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int sb = b & 1;
             const float sk_b = sk_next;
             if (b + 1 < nb) sk_next = skh[b + 1];
-            ok = __all_sync(0xffffffffu, mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns));
-            if (!ok) break;
+            bool wok = mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns);
             // PV(b-2) and its row sums are done (also frees P buffer sb)
-            if (b >= 2) {
-                ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns));
-                if (!ok) break;
-            }
-            tc_fence_after();
-            uint32_t S[128];
+            if (b >= 2) wok = wok && mbar_wait(B.pv_done + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns);
+            wok = __all_sync(0xffffffffu, wok) && ok;
+            uint32_t S[64];
             uint32_t rs_raw = 0;
-            const uint32_t tS = tmem + lane_base + sb * 128;
-            VCA_TMEM_LD32(tS + 0, (S + 0));
-            VCA_TMEM_LD32(tS + 32, (S + 32));
-            VCA_TMEM_LD32(tS + 64, (S + 64));
-            VCA_TMEM_LD32(tS + 96, (S + 96));
-            if (b >= 2) {
-                const uint32_t trs = tmem + lane_base + kTmemRS + 16 * ((b - 2) % kRsSlots);
-                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(trs));
-            }
-            tmem_ld_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.s_free + sb);
-
+            float pm = kNegInf;
             const float c = __fmul_rn(__fmul_rn(sqv, sk_b), p.scale_log2);
-            float a0 = __uint_as_float(S[0]), a1 = __uint_as_float(S[1]);
-            float a2 = __uint_as_float(S[2]), a3 = __uint_as_float(S[3]);
-#pragma unroll
-            for (int j = 4; j < 128; j += 8) {
-                a0 = max3(a0, __uint_as_float(S[j + 0]), __uint_as_float(S[j + 1]));
-                a1 = max3(a1, __uint_as_float(S[j + 2]), __uint_as_float(S[j + 3]));
-                a2 = max3(a2, __uint_as_float(S[j + 4]), __uint_as_float(S[j + 5]));
-                a3 = max3(a3, __uint_as_float(S[j + 6]), __uint_as_float(S[j + 7]));
-            }
-            const float smax = fmaxf(max3(a0, a1, a2), a3);
-            const float m_new = fmaxf(m, __fmul_rn(smax, c));
-            float alpha = 1.0f;
-            if (m_new > m && b > 0) alpha = ex2_approx(__fsub_rn(m, m_new));
-            m = m_new;
-            const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
-            if (alpha != 1.0f) {
-                l = __fmul_rn(l, alpha);
-#pragma unroll 1
-                for (int i = 0; i < rs_cnt; ++i) sRS[i * kBlk + row] = __fmul_rn(sRS[i * kBlk + row], alpha);
-            }
-            if (b >= 2) {
-                // row sum of block b-2, taken against that block's max: bring it to m
-                float rs = __uint_as_float(rs_raw);
-                if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
-                l = __fadd_rn(l, rs);
-                sRS[rs_cnt * kBlk + row] = rs;
-                ++rs_cnt;
-            }
-
             unsigned char *prow = sP + sb * kTileBytes;
-            if constexpr (kExpcast) {
-                const float c8 = __fmul_rn(8.0f, c);
-                const float bias = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m));
-                const uint64_t c8x2 = pk2(__float_as_uint(c8), __float_as_uint(c8));
-                const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
-                const uint64_t mx2 = pk2(__float_as_uint(kMagic), __float_as_uint(kMagic));
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t *s = S + ch * 16;
-                    const uint32_t w0 = expcast4(s[0], s[1], s[2], s[3], c8x2, bx2, mx2);
-                    const uint32_t w1 = expcast4(s[4], s[5], s[6], s[7], c8x2, bx2, mx2);
-                    const uint32_t w2 = expcast4(s[8], s[9], s[10], s[11], c8x2, bx2, mx2);
-                    const uint32_t w3 = expcast4(s[12], s[13], s[14], s[15], c8x2, bx2, mx2);
-                    *reinterpret_cast<uint4 *>(prow + sw128_offset(row, ch)) = make_uint4(w0, w1, w2, w3);
+            if (wok) {
+                tc_fence_after();
+                const uint32_t tS = tmem + lane_base + sb * 128 + col0;
+                VCA_TMEM_LD32(tS + 0, (S + 0));
+                VCA_TMEM_LD32(tS + 32, (S + 32));
+                if (half == 0 && b >= 2) {
+                    const uint32_t trs = tmem + lane_base + kTmemRS + 16 * ((b - 2) % kRsSlots);
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(trs));
                 }
-            } else {
-                const float negm = -m;
-                const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
-                const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
+                tmem_ld_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B.s_free + sb);
+                float a[4] = {__uint_as_float(S[0]), __uint_as_float(S[1]), __uint_as_float(S[2]),
+                              __uint_as_float(S[3])};
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    const uint32_t *s = S + ch * 16;
-                    const uint32_t w0 = expconv4(s[0], s[1], s[2], s[3], cx2, nx2);
-                    const uint32_t w1 = expconv4(s[4], s[5], s[6], s[7], cx2, nx2);
-                    const uint32_t w2 = expconv4(s[8], s[9], s[10], s[11], cx2, nx2);
-                    const uint32_t w3 = expconv4(s[12], s[13], s[14], s[15], cx2, nx2);
-                    *reinterpret_cast<uint4 *>(prow + sw128_offset(row, ch)) = make_uint4(w0, w1, w2, w3);
+                for (int j = 4; j < 64; j += 2)
+                    a[(j >> 1) & 3] = max3(a[(j >> 1) & 3], __uint_as_float(S[j]), __uint_as_float(S[j + 1]));
+                pm = fmaxf(max3(a[0], a[1], a[2]), a[3]);
+                sPM[(sb * 2 + half) * kBlk + row] = pm;
+                // codes against the current reference max, on the bet that this
+                // block does not move it (rewritten below when it does)
+                if (b > 0) write_codes<kExpcast>(S, c, m, prow, row, half);
+            }
+            ok = bar_and(wok, pair_bar, 64);
+            if (!ok) break;
+            const float smax = fmaxf(pm, sPM[(sb * 2 + (half ^ 1)) * kBlk + row]);
+            const float bm = __fmul_rn(smax, c);
+            // lazy reference-max update: only when the block's max exceeds it by tau
+            const bool moved = bm > __fadd_rn(m, kLazyTau);
+            float alpha = 1.0f;
+            if (moved) {
+                if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
+                m = bm;
+            }
+            if (__any_sync(0xffffffffu, moved)) write_codes<kExpcast>(S, c, m, prow, row, half);
+            const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
+            if (half == 0) {
+                if (alpha != 1.0f) {
+                    l = __fmul_rn(l, alpha);
+#pragma unroll 1
+                    for (int i = 0; i < rs_cnt; ++i) sRS[i * kBlk + row] = __fmul_rn(sRS[i * kBlk + row], alpha);
+                }
+                if (b >= 2) {
+                    // row sum of block b-2, taken against that block's max: bring it to m
+                    float rs = __uint_as_float(rs_raw);
+                    if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
+                    l = __fadd_rn(l, rs);
+                    sRS[rs_cnt * kBlk + row] = rs;
                 }
             }
+            if (b >= 2) ++rs_cnt;
 
-            // rescale the O accumulator after PV(b-1) (and any mean MMA after it) finished
+            // rescale this half of the O accumulator after PV(b-1) (and any mean
+            // MMA after it) finished
             if (rescale) {
                 const int jb = b - 1;
                 ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + (jb & 1), (jb >> 1) & 1, abort_flag, p.limit_ns));
-                if (!ok) break;
-                tc_fence_after();
+                if (ok) {
+                    tc_fence_after();
 #pragma unroll 1
-                for (int i = 0; i < 4; ++i) {
-                    uint32_t o[32];
-                    VCA_TMEM_LD32(tO + 32 * i, o);
-                    tmem_ld_wait();
+                    for (int i = 0; i < 2; ++i) {
+                        uint32_t o[32];
+                        VCA_TMEM_LD32(tO + 32 * i, o);
+                        tmem_ld_wait();
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
-                    VCA_TMEM_ST32(tO + 32 * i, o);
+                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
+                        VCA_TMEM_ST32(tO + 32 * i, o);
+                    }
+                    tmem_st_wait();
                 }
-                tmem_st_wait();
             }
 
-            if (flush_after(b)) {
+            if (ok && flush_after(b)) {
                 // row sums of blocks b0 .. b0+15 (all at the current max):
-                // A row (this query row): [rs hi | rs lo | rs hi | rs lo]
-                // B row (channel `row`):  [mu hi | mu hi | mu lo | mu lo], mu = mean / s_v
+                // A row (query row, half 0):  [rs hi | rs lo | rs hi | rs lo]
+                // B row (channel `row`, half 1): [mu hi | mu hi | mu lo | mu lo], mu = mean / s_v
                 const int b0 = b - kMeanJ - 1;
-                const float inv_sv = 1.0f / sSV[row];
-                float rh[kMeanJ], rl[kMeanJ], mh[kMeanJ], ml[kMeanJ];
+                float hi[kMeanJ], lo[kMeanJ];
+                if (half == 0) {
 #pragma unroll
-                for (int i = 0; i < kMeanJ; ++i) {
-                    split_bf16(sRS[i * kBlk + row], rh[i], rl[i]);
-                    split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), mh[i], ml[i]);
+                    for (int i = 0; i < kMeanJ; ++i) split_bf16(sRS[i * kBlk + row], hi[i], lo[i]);
+                } else {
+                    const float inv_sv = 1.0f / sSV[row];
+#pragma unroll
+                    for (int i = 0; i < kMeanJ; ++i)
+                        split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
+                }
+                unsigned char *dst = half == 0 ? sMA : sMB;
+                uint4 hv[2], lv[2];
+#pragma unroll
+                for (int g = 0; g < 2; ++g) {
+                    hv[g] = make_uint4(pack_bf16x2(hi[8 * g + 0], hi[8 * g + 1]), pack_bf16x2(hi[8 * g + 2], hi[8 * g + 3]),
+                                       pack_bf16x2(hi[8 * g + 4], hi[8 * g + 5]), pack_bf16x2(hi[8 * g + 6], hi[8 * g + 7]));
+                    lv[g] = make_uint4(pack_bf16x2(lo[8 * g + 0], lo[8 * g + 1]), pack_bf16x2(lo[8 * g + 2], lo[8 * g + 3]),
+                                       pack_bf16x2(lo[8 * g + 4], lo[8 * g + 5]), pack_bf16x2(lo[8 * g + 6], lo[8 * g + 7]));
                 }
 #pragma unroll
                 for (int ck = 0; ck < 8; ++ck) {
-                    const float *srcA = ((ck >> 1) & 1) ? rl : rh;   // chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo
-                    const float *srcB = (ck < 4) ? mh : ml;          // chunks 0-3 hi; 4-7 lo
-                    const int i0 = (ck & 1) * 8;
-                    uint4 a, bv;
-                    a.x = pack_bf16x2(srcA[i0 + 0], srcA[i0 + 1]);
-                    a.y = pack_bf16x2(srcA[i0 + 2], srcA[i0 + 3]);
-                    a.z = pack_bf16x2(srcA[i0 + 4], srcA[i0 + 5]);
-                    a.w = pack_bf16x2(srcA[i0 + 6], srcA[i0 + 7]);
-                    bv.x = pack_bf16x2(srcB[i0 + 0], srcB[i0 + 1]);
-                    bv.y = pack_bf16x2(srcB[i0 + 2], srcB[i0 + 3]);
-                    bv.z = pack_bf16x2(srcB[i0 + 4], srcB[i0 + 5]);
-                    bv.w = pack_bf16x2(srcB[i0 + 6], srcB[i0 + 7]);
-                    *reinterpret_cast<uint4 *>(sMA + sw128_offset(row, ck)) = a;
-                    *reinterpret_cast<uint4 *>(sMB + sw128_offset(row, ck)) = bv;
+                    // A: chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo.   B: chunks 0-3 hi; 4-7 lo.
+                    const bool use_lo = (half == 0) ? (((ck >> 1) & 1) != 0) : (ck >= 4);
+                    *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ck)) = use_lo ? lv[ck & 1] : hv[ck & 1];
                 }
                 rs_cnt = 0;
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.p_full + sb);
+            if (ok) {
+                fence_proxy_async_smem();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B.p_full + sb);
+            }
             mh2 = mh1;
             mh1 = m;
         }
@@ -466,54 +476,56 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + (jb & 1), (jb >> 1) & 1, abort_flag, p.limit_ns));
         }
         // every softmax warp arrives here, whether it finished or gave up; the
-        // epilogue (and its named barrier) runs only if all four finished
-        ok = softmax_all(ok);
+        // epilogue (and its barriers) runs only if all of them finished
+        ok = bar_and(ok, kBarSoftmax, 32 * kSoftmaxWarps);
         if (ok) {
             tc_fence_after();
-            // the last two blocks' row sums
-            uint32_t r2 = 0, r1 = 0;
-            const uint32_t tr = tmem + lane_base + kTmemRS;
-            if (nb >= 2)
+            if (half == 0) {
+                // the last two blocks' row sums
+                uint32_t r2 = 0, r1 = 0;
+                const uint32_t tr = tmem + lane_base + kTmemRS;
+                if (nb >= 2)
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                                 : "=r"(r2) : "r"(tr + 16 * ((nb - 2) % kRsSlots)));
                 asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
-                             : "=r"(r2) : "r"(tr + 16 * ((nb - 2) % kRsSlots)));
-            asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
-                         : "=r"(r1) : "r"(tr + 16 * ((nb - 1) % kRsSlots)));
-            tmem_ld_wait();
-            if (nb >= 2) {
-                float rs = __uint_as_float(r2);
-                if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
-                l = __fadd_rn(l, rs);
-                sRS[rs_cnt * kBlk + row] = rs;
-                ++rs_cnt;
-            }
-            {
+                             : "=r"(r1) : "r"(tr + 16 * ((nb - 1) % kRsSlots)));
+                tmem_ld_wait();
+                int cnt = rs_cnt;
+                if (nb >= 2) {
+                    float rs = __uint_as_float(r2);
+                    if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
+                    l = __fadd_rn(l, rs);
+                    sRS[cnt * kBlk + row] = rs;
+                    ++cnt;
+                }
                 const float rs = __uint_as_float(r1);   // taken against m itself
                 l = __fadd_rn(l, rs);
-                sRS[rs_cnt * kBlk + row] = rs;
-                ++rs_cnt;
+                sRS[cnt * kBlk + row] = rs;
+                sL[row] = l;
             }
+            rs_cnt += (nb >= 2) ? 2 : 1;
             // the blocks since the last mean MMA: stage their means (fp32) in the
             // mean-B buffer, whose last reader (the final mean MMA) has finished
             const int tail0 = nb - rs_cnt;
             float *sMu = reinterpret_cast<float *>(sMB);
-            softmax_bar();
-            for (int i = threadIdx.x - 64; i < rs_cnt * kD; i += 128)
+            bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
+            for (int i = threadIdx.x - 64; i < rs_cnt * kD; i += 32 * kSoftmaxWarps)
                 sMu[i] = bf16_bits_to_f32(vmh[(tail0 + i / kD) * kD + (i % kD)]);
-            softmax_bar();
-            const float inv_l = 1.0f / l;
-            uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD;
+            bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
+            const float inv_l = 1.0f / sL[row];
+            uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD + col0;
 #pragma unroll 1
-            for (int i = 0; i < 4; ++i) {
+            for (int i = 0; i < 2; ++i) {
                 uint32_t o[32];
                 VCA_TMEM_LD32(tO + 32 * i, o);
                 tmem_ld_wait();
                 float acc[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = __fmul_rn(__uint_as_float(o[e]), sSV[32 * i + e]);
+                for (int e = 0; e < 32; ++e) acc[e] = __fmul_rn(__uint_as_float(o[e]), sSV[col0 + 32 * i + e]);
 #pragma unroll 1
                 for (int t = 0; t < rs_cnt; ++t) {
                     const float r = sRS[t * kBlk + row];
-                    const float *mu = sMu + t * kD + 32 * i;
+                    const float *mu = sMu + t * kD + col0 + 32 * i;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) acc[e] = __fmaf_rn(r, mu[e], acc[e]);
                 }
@@ -572,13 +584,30 @@ bool make_tile_map(CUtensorMap *map, const void *base, uint64_t rows) {
 }
 
 // ExpCast map alone, for bit-exact tests of the device function.
+// Four elements per thread through the same packed path the attention kernel
+// uses.  The unclipped variant is taken where the attention kernel would take
+// it: |m| < 2^22 and fp32(s_raw * c) <= fp32(m + 8) (m is the lazily updated
+// reference max there).
 __global__ void expcast_codes_kernel(const float *__restrict__ s_raw, const float *__restrict__ c,
                                      const float *__restrict__ m, int64_t n, uint8_t *__restrict__ out) {
-    for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const float c8 = __fmul_rn(8.0f, c[i]);
-        const float bias = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m[i]));
-        out[i] = static_cast<uint8_t>(expcast_code(s_raw[i], c8, bias));
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; 4 * g < n;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        uint32_t sv[4], c8[4], bias[4];
+        bool fast = true;
+        for (int e = 0; e < 4; ++e) {
+            const int64_t i = (4 * g + e < n) ? 4 * g + e : n - 1;
+            sv[e] = __float_as_uint(s_raw[i]);
+            c8[e] = __float_as_uint(__fmul_rn(8.0f, c[i]));
+            bias[e] = __float_as_uint(__fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m[i])));
+            fast = fast && fabsf(m[i]) < kExpcastFastMax && __fmul_rn(s_raw[i], c[i]) <= __fadd_rn(m[i], 8.0f);
+        }
+        const uint64_t s01 = pk2(sv[0], sv[1]), s23 = pk2(sv[2], sv[3]);
+        const uint32_t w = fast ? expcast4<false>(s01, s23, pk2(c8[0], c8[1]), pk2(c8[2], c8[3]),
+                                                  pk2(bias[0], bias[1]), pk2(bias[2], bias[3]))
+                                : expcast4<true>(s01, s23, pk2(c8[0], c8[1]), pk2(c8[2], c8[3]),
+                                                 pk2(bias[0], bias[1]), pk2(bias[2], bias[3]));
+        for (int e = 0; e < 4; ++e)
+            if (4 * g + e < n) out[4 * g + e] = static_cast<uint8_t>((w >> (8 * e)) & 0xFFu);
     }
 }
 

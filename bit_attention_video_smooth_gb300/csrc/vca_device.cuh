@@ -63,6 +63,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// try_wait that may suspend the thread (up to `hint_ns`) until the phase
+// completes, instead of returning at once: waiting warps then stop competing
+// for issue slots with the warps doing the work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait until the phase with the given parity of `bar` has completed, or give
 // up: after `limit_ns` of wall time, or as soon as another thread of the CTA
 // has raised `*abort`.  Returns false on giving up (and raises *abort).
@@ -71,8 +86,8 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *a
     const uint64_t t0 = globaltimer_ns();
     while (true) {
 #pragma unroll 1
-        for (int i = 0; i < 32; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        for (int i = 0; i < 8; ++i)
+            if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
         if (*reinterpret_cast<volatile int *>(abort)) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *reinterpret_cast<volatile int *>(abort) = 1;
@@ -247,6 +262,59 @@ __device__ __forceinline__ uint32_t expcast_code(float s_raw, float c8, float bi
 // the fp32 pattern of a normal E4M3 value; the flushed code decodes to 0.
 __device__ __forceinline__ float expcast_value(float x) {
     return (x == kMagic) ? 0.0f : __uint_as_float((__float_as_uint(x) << 20) + 0x3C000000u);
+}
+
+// Packed fp32 pairs: two lanes per instruction on sm_100 and later.
+__device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(hi));
+    return d;
+}
+__device__ __forceinline__ void upk2(uint64_t v, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+__device__ __forceinline__ uint64_t add2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// Byte permute with the selector's sign-replication bit honoured.
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Four ExpCast codes packed in one word (byte i = element i), the same
+// arithmetic as expcast_rounded(): per element one fp32 FMA t = fma(s, 8c, bias)
+// (packed two per instruction), rounding to an integer by adding 1.5 * 2^23,
+// then the clip: codes below 0 (and NaN) become 0 with one max, codes above 126
+// become 126 (kClip), and the bytes 1..7 are zeroed together: a byte b <= 126
+// is >= 8 exactly when b + 120 has its top bit set, which PRMT replicates into
+// a byte mask.  Without kClip the caller guarantees codes <= 126: that holds
+// when fp32(s * c) <= fp32(m + 8) and |m| < 2^22, because t then exceeds
+// 55.65 by at most 8 * 8 + 16 ulp(m) <= 68.
+constexpr float kExpcastFastMax = 4194304.0f;   // 2^22
+template <bool kClip>
+__device__ __forceinline__ uint32_t expcast4(uint64_t s01, uint64_t s23, uint64_t c8_01, uint64_t c8_23,
+                                             uint64_t b01, uint64_t b23) {
+    const uint64_t magic2 = pk2(__float_as_uint(kMagic), __float_as_uint(kMagic));
+    float x[4];
+    upk2(add2(fma2(s01, c8_01, b01), magic2), x[0], x[1]);
+    upk2(add2(fma2(s23, c8_23, b23), magic2), x[2], x[3]);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        x[e] = fmaxf(x[e], kMagic);
+        if (kClip) x[e] = fminf(x[e], kMagic + 126.0f);
+    }
+    const uint32_t w = prmt(prmt(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x0040),
+                            prmt(__float_as_uint(x[2]), __float_as_uint(x[3]), 0x0040), 0x5410);
+    return w & prmt(w + 0x78787878u, 0u, 0xBA98);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {

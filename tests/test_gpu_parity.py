@@ -58,7 +58,13 @@ def test_expcast_codes_bit_exact(V, orc):
     edge_s = np.array([0.0, 0.0, 0.0, 1.0, -1.0, 20.0, np.inf, -np.inf, np.nan, 1e30], np.float32)
     edge_c = np.ones_like(edge_s)
     edge_m = np.array([0.0, 6.01875, 6.0187, -10.0, 0.0, 0.0, 0.0, 0.0, 0.0, 0.0], np.float32)
-    s, c, m = (np.concatenate([a, b]) for a, b in ((s, edge_s), (c, edge_c), (m, edge_m)))
+    # running maxima beyond 2^26, where the FMA's rounding can push codes past
+    # 126 and the clip matters (the kernel's slow path)
+    big_m = np.repeat(np.array([1e8, -3e8, 3e9], np.float32), 4096)
+    big_s = (big_m.astype(np.float64) * (1 + rng.uniform(-3e-7, 3e-7, big_m.size))).astype(np.float32)
+    big_c = np.ones_like(big_m)
+    s, c, m = (np.concatenate([a, b, e]) for a, b, e in
+               ((s, edge_s, big_s), (c, edge_c, big_c), (m, edge_m, big_m)))
     ref = orc.expcast_codes(s, c, m)
     out = torch.empty(s.size, dtype=torch.uint8, device="cuda")
     V.vca_expcast_codes(_dev(s), _dev(c), _dev(m), out)
