@@ -6,14 +6,15 @@
 //
 // One CTA owns a 128-row query tile of one (batch, head) and streams the key
 // blocks of that head in increasing (permuted) order.  Warp roles:
-//   warp 0     TMA producer: Q once, then K / V-residual tiles into a 3-stage ring
-//   warp 1     TMEM owner and MMA issuer (one thread), per key block b:
-//                S[b&1] = Q8 K8_b^T                       (kind::f8f6f4, N = 128)
-//                O     += P_{b-1} V8_{b-1}                 (kind::f8f6f4, N = 128)
-//                RS[(b-1)%8] = P_{b-1} 1                   (kind::f8f6f4, N = 16)
-//              the last one writes the block's row sums of the decoded P into a
-//              rotating TMEM slot, so the softmax threads never add them up; and
-//              every 16 key blocks O += [rowsum hi|lo] [mean/s_v hi|lo]^T (bf16).
+//   warp 0     TMA producer: Q once, then K tiles into a 4-stage ring
+//   warp 10    TMA producer: V-residual tiles into a 3-stage ring
+//   warp 1     TMEM owner and MMA issuer (one thread):
+//                S[b&1] = Q8 K8_b^T                 (kind::f8f6f4, N = 128), issued
+//                         two blocks ahead, once the softmax has read S[b&1]
+//                [E | O] += P_b [ones ; V8_b]       (kind::f8f6f4, N = 144): the
+//                         16 extra output columns are the block's row sums of the
+//                         decoded P, so the softmax threads never add them up
+//              and every 16 key blocks O += [rowsum hi|lo] [mean/s_v hi|lo]^T (bf16).
 //   warps 2-9  softmax: two threads per query row -- the warps w and w+4 share
 //              a TMEM lane quarter and take the S columns 0-63 and 64-127; the
 //              pair exchanges its half-row maxima through shared memory at a
@@ -23,7 +24,7 @@
 //              block b-2 is read from its TMEM slot, brought to the current max
 //              and buffered for the mean restore; epilogue O = (O s_v + the
 //              last, partial group of mean terms) / l.
-// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), row-sum slots [384,512).
+// TMEM columns: S0 [0,128), S1 [128,256), E0 [256,272), O [272,400), E1 [400,416).
 // Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
 // drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
 #include <cuda.h>
@@ -35,35 +36,41 @@ namespace vca {
 
 namespace {
 
-constexpr int kStages = 3;
+constexpr int kKStages = 3;               // K tiles in flight (released after their QK MMA)
+constexpr int kVStages = 3;               // V tiles in flight (released after their PV MMA)
 constexpr int kSoftmaxWarps = 8;
-constexpr int kThreads = 64 + 32 * kSoftmaxWarps;
+constexpr int kVWarp = 2 + kSoftmaxWarps;  // the V producer
+constexpr int kThreads = 32 * (kVWarp + 1);
 constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
-constexpr int kRsSlots = 8;                // rotating TMEM row-sum slots (16 columns each)
 constexpr int kRsCap = 32;                 // buffered row sums per row (<= 17 in use)
 constexpr uint32_t kTileBytes = kBlk * kD; // one 128 x 128 FP8 tile (16 KB)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256, kTmemRS = 384;
+// TMEM: S0 [0,128), S1 [128,256), row-sum slot E0 [256,272), O [272,400), E1 [400,416).
+// PV of an even block writes [E0 | O] (B = [ones ; V]), of an odd block [O | E1]
+// (B = [V ; ones]): the 16 extra output columns are the block's row sums.
+constexpr uint32_t kTmemE0 = 256, kTmemO = 272, kTmemE1 = 400;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t kOffQ = 0;
 constexpr uint32_t kOffK = kOffQ + kTileBytes;
-constexpr uint32_t kOffV = kOffK + kStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kStages * kTileBytes;
+constexpr uint32_t kOnesBytes = 16 * 128;            // 16 rows of E4M3 1.0
+constexpr uint32_t kVStageBytes = kOnesBytes + kTileBytes + kOnesBytes;   // [ones | V | ones]
+constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kOffP = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kOffMA = kOffP + 2 * kTileBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
-constexpr uint32_t kOffOnes = kOffMB + kTileBytes;          // 16 x 128 E4M3 ones (B of the row-sum MMA)
-constexpr uint32_t kOffRS = kOffOnes + 16 * 128;            // fp32 [kRsCap][128] buffered row sums
+constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128] buffered row sums
 constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residual scales
 constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][2][128] half-row maxima
 constexpr uint32_t kOffL = kOffPM + 4 * kBlk * 4;           // fp32 [128] final row sums
 constexpr uint32_t kOffBar = kOffL + kBlk * 4;
-constexpr int kNumBars = 1 + 3 * kStages + 2 * 4 + 1;
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t *q_full, *k_full, *v_full, *kv_empty, *s_full, *s_free, *p_full, *pv_done, *drain;
+    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *pv_done, *drain;
 };
 
 struct Params {
@@ -194,9 +201,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars B;
     B.q_full = bars;
     B.k_full = bars + 1;
-    B.v_full = B.k_full + kStages;
-    B.kv_empty = B.v_full + kStages;
-    B.s_full = B.kv_empty + kStages;
+    B.k_empty = B.k_full + kKStages;
+    B.v_full = B.k_empty + kKStages;
+    B.v_empty = B.v_full + kVStages;
+    B.s_full = B.v_empty + kVStages;
     B.s_free = B.s_full + 2;
     B.p_full = B.s_free + 2;
     B.pv_done = B.p_full + 2;
@@ -214,10 +222,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(B.q_full, 1);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < kKStages; ++s) {
             mbar_init(B.k_full + s, 1);
+            mbar_init(B.k_empty + s, 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
             mbar_init(B.v_full + s, 1);
-            mbar_init(B.kv_empty + s, 1);
+            mbar_init(B.v_empty + s, 1);
         }
         for (int i = 0; i < 2; ++i) {
             mbar_init(B.s_full + i, 1);
@@ -236,8 +247,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 2 && warp < 6) {
         const int t = threadIdx.x - 64;
         sSV[t] = p.v_scale[static_cast<int64_t>(bh) * kD + t];
-        // the ones tile: 16 rows x 128 bytes of E4M3 1.0 (0x38)
-        *reinterpret_cast<uint4 *>(smem + kOffOnes + 16 * t) = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        // the ones rows around every V stage: 16 x 128 bytes of E4M3 1.0 (0x38)
+        const uint4 ones = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
+        for (int st = 0; st < kVStages; ++st) {
+            unsigned char *vs = smem + kOffV + st * kVStageBytes;
+            *reinterpret_cast<uint4 *>(vs + 16 * t) = ones;
+            *reinterpret_cast<uint4 *>(vs + kOnesBytes + kTileBytes + 16 * t) = ones;
+        }
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -245,79 +261,88 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == kVWarp) {
+        // ------------------------------------------------------------ producers
+        // warp 0: Q once, then the K ring; warp kVWarp: the V ring.  The rings
+        // are independent, so a K tile is requested as soon as the QK MMA of
+        // the tile it replaces is done (not only after that block's PV).
         if (lane == 0) {
-            tma_prefetch_desc(&tmQ);
-            tma_prefetch_desc(&tmK);
-            tma_prefetch_desc(&tmV);
-            int armed[kStages];
-            for (int s = 0; s < kStages; ++s) armed[s] = 0;
-            mbar_expect_tx(B.q_full, kTileBytes);
-            tma_load_2d(smem + kOffQ, &tmQ, B.q_full, 0, bh * N + qtile * kBlk);
+            const bool is_k = (warp == 0);
+            const int stages = is_k ? kKStages : kVStages;
+            uint64_t *full = is_k ? B.k_full : B.v_full;
+            uint64_t *empty = is_k ? B.k_empty : B.v_empty;
+            unsigned char *ring = smem + (is_k ? kOffK : kOffV + kOnesBytes);
+            const uint32_t stride = is_k ? kTileBytes : kVStageBytes;
+            const void *tm = is_k ? static_cast<const void *>(&tmK) : static_cast<const void *>(&tmV);
+            tma_prefetch_desc(tm);
+            int armed[kKStages > kVStages ? kKStages : kVStages];
+            for (int s = 0; s < stages; ++s) armed[s] = 0;
+            if (is_k) {
+                tma_prefetch_desc(&tmQ);
+                mbar_expect_tx(B.q_full, kTileBytes);
+                tma_load_2d(smem + kOffQ, &tmQ, B.q_full, 0, bh * N + qtile * kBlk);
+            }
             for (int b = 0; b < nb; ++b) {
-                const int s = b % kStages, use = b / kStages;
-                if (use > 0 && !mbar_wait(B.kv_empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) break;
-                mbar_expect_tx(B.k_full + s, kTileBytes);
-                tma_load_2d(smem + kOffK + s * kTileBytes, &tmK, B.k_full + s, 0, bh * N + b * kBlk);
-                mbar_expect_tx(B.v_full + s, kTileBytes);
-                tma_load_2d(smem + kOffV + s * kTileBytes, &tmV, B.v_full + s, 0, (bh * nb + b) * kBlk);
+                const int s = b % stages, use = b / stages;
+                if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) break;
+                mbar_expect_tx(full + s, kTileBytes);
+                tma_load_2d(ring + s * stride, tm, full + s, 0, is_k ? bh * N + b * kBlk : (bh * nb + b) * kBlk);
                 armed[s] = use + 1;
             }
             // every copy this thread issued has landed before the CTA can exit
-            drain_wait(B.q_full, 0, p.limit_ns);
-            for (int s = 0; s < kStages; ++s)
-                if (armed[s] > 0) {
-                    drain_wait(B.k_full + s, (armed[s] - 1) & 1, p.limit_ns);
-                    drain_wait(B.v_full + s, (armed[s] - 1) & 1, p.limit_ns);
-                }
+            if (is_k) drain_wait(B.q_full, 0, p.limit_ns);
+            for (int s = 0; s < stages; ++s)
+                if (armed[s] > 0) drain_wait(full + s, (armed[s] - 1) & 1, p.limit_ns);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc_f8 = make_idesc(128, 128, 0, 0);
-            constexpr uint32_t idesc_rs = make_idesc(128, 16, 0, 0);
+            constexpr uint32_t idesc_qk = make_idesc(128, 128, 0, 0);
+            constexpr uint32_t idesc_pv = make_idesc(128, 144, 0, 0);
             constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
             const uint32_t sbase = smem_u32(smem);
             const uint64_t dq = sdesc_k_sw128(sbase + kOffQ);
             const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
             const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
-            const uint64_t dones = sdesc_k_sw128(sbase + kOffOnes);
             const uint32_t tO = tmem + kTmemO;
+            // QK(b) -> S[b & 1]; needs K(b) and S[b & 1] released by the softmax of b-2
+            auto issue_qk = [&](int b) -> bool {
+                const int s = b % kKStages, sb = b & 1;
+                if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) return false;
+                if (b >= 2 && !mbar_wait(B.s_free + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns)) return false;
+                tc_fence_after();
+                const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
+#pragma unroll
+                for (int kk = 0; kk < kD / 32; ++kk)
+                    mma_f8f6f4(tmem + sb * 128, dq + 2 * kk, dk + 2 * kk, idesc_qk, kk > 0);
+                tc_commit(B.k_empty + s);
+                tc_commit(B.s_full + sb);
+                return true;
+            };
             bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
-            for (int b = 0; ok && b <= nb; ++b) {
-                if (b < nb) {
-                    const int s = b % kStages, sb = b & 1;
-                    if (!mbar_wait(B.k_full + s, (b / kStages) & 1, abort_flag, p.limit_ns)) break;
-                    if (b >= 2 && !mbar_wait(B.s_free + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns)) break;
-                    tc_fence_after();
-                    const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
+            ok = ok && issue_qk(0);
+            if (nb > 1) ok = ok && issue_qk(1);
+            for (int j = 0; ok && j < nb; ++j) {
+                // QK two blocks ahead, as soon as the softmax has read S(j)
+                if (j + 2 < nb && !issue_qk(j + 2)) break;
+                // PV(j): O (+)= P_j V_j with the block's row sums in the extra 16 columns
+                const int s = j % kVStages, pb = j & 1;
+                if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
+                if (!mbar_wait(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
+                tc_fence_after();
+                const uint64_t dp = sdesc_k_sw128(sbase + kOffP + pb * kTileBytes);
+                const uint32_t vstage = sbase + kOffV + s * kVStageBytes;
+                const uint64_t dv = sdesc_k_sw128(pb == 0 ? vstage : vstage + kOnesBytes);
+                const uint32_t td = tmem + (pb == 0 ? kTmemE0 : kTmemO);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 32; ++kk)
-                        mma_f8f6f4(tmem + sb * 128, dq + 2 * kk, dk + 2 * kk, idesc_f8, kk > 0);
-                    tc_commit(B.s_full + sb);
+                for (int kk = 0; kk < kBlk / 32; ++kk)
+                    mma_f8f6f4(td, dp + 2 * kk, dv + 2 * kk, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                if (flush_after(j)) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
                 }
-                if (b >= 1) {
-                    const int j = b - 1, s = j % kStages, pb = j & 1;
-                    if (!mbar_wait(B.v_full + s, (j / kStages) & 1, abort_flag, p.limit_ns)) break;
-                    if (!mbar_wait(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
-                    tc_fence_after();
-                    const uint64_t dp = sdesc_k_sw128(sbase + kOffP + pb * kTileBytes);
-                    const uint64_t dv = sdesc_k_sw128(sbase + kOffV + s * kTileBytes);
-#pragma unroll
-                    for (int kk = 0; kk < kBlk / 32; ++kk)
-                        mma_f8f6f4(tO, dp + 2 * kk, dv + 2 * kk, idesc_f8, (j > 0 || kk > 0) ? 1u : 0u);
-                    const uint32_t trs = tmem + kTmemRS + 16 * (j % kRsSlots);
-#pragma unroll
-                    for (int kk = 0; kk < kBlk / 32; ++kk)
-                        mma_f8f6f4(trs, dp + 2 * kk, dones + 2 * kk, idesc_rs, kk > 0 ? 1u : 0u);
-                    if (flush_after(j)) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
-                    }
-                    tc_commit(B.kv_empty + s);
-                    tc_commit(B.pv_done + pb);
-                }
+                tc_commit(B.v_empty + s);
+                tc_commit(B.pv_done + pb);
             }
             tc_commit(B.drain);
             drain_wait(B.drain, 0, p.limit_ns);
@@ -361,11 +386,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t tS = tmem + lane_base + sb * 128 + col0;
                 VCA_TMEM_LD32(tS + 0, (S + 0));
                 VCA_TMEM_LD32(tS + 32, (S + 32));
-                if (half == 0 && b >= 2) {
-                    const uint32_t trs = tmem + lane_base + kTmemRS + 16 * ((b - 2) % kRsSlots);
-                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(trs));
-                }
+                // half 0 owns the row-sum slot of this parity: read block b-2's
+                // sum, then clear the slot for PV(b) (PV(0) initialises E0 itself)
+                const uint32_t te = tmem + lane_base + (sb == 0 ? kTmemE0 : kTmemE1);
+                if (half == 0 && b >= 2)
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
                 tmem_ld_wait();
+                if (half == 0 && b >= 1) {
+                    asm volatile(
+                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
+                        ::"r"(te), "r"(0u) : "memory");
+                    tmem_st_wait();
+                }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(B.s_free + sb);
@@ -483,12 +515,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (half == 0) {
                 // the last two blocks' row sums
                 uint32_t r2 = 0, r1 = 0;
-                const uint32_t tr = tmem + lane_base + kTmemRS;
+                const uint32_t te0 = tmem + lane_base + kTmemE0, te1 = tmem + lane_base + kTmemE1;
+                const uint32_t te_last = ((nb - 1) & 1) ? te1 : te0, te_prev = ((nb - 1) & 1) ? te0 : te1;
                 if (nb >= 2)
-                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
-                                 : "=r"(r2) : "r"(tr + 16 * ((nb - 2) % kRsSlots)));
-                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
-                             : "=r"(r1) : "r"(tr + 16 * ((nb - 1) % kRsSlots)));
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r2) : "r"(te_prev));
+                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r1) : "r"(te_last));
                 tmem_ld_wait();
                 int cnt = rs_cnt;
                 if (nb >= 2) {
