@@ -6,11 +6,11 @@
 //
 // One CTA owns a 128-row query tile of one (batch, head) and streams the key
 // blocks of that head in increasing (permuted) order.  Warp roles:
-//   warp 0     TMA producer: Q once, then K tiles into a 4-stage ring
+//   warp 0     TMA producer: K tiles into a 3-stage ring
 //   warp 10    TMA producer: V-residual tiles into a 3-stage ring
 //   warp 1     TMEM owner and MMA issuer (one thread):
 //                S[b&1] = Q8 K8_b^T                 (kind::f8f6f4, N = 128), issued
-//                         two blocks ahead, once the softmax has read S[b&1]
+//                         right after PV(b-2)
 //                [E | O] += P_b [ones ; V8_b]       (kind::f8f6f4, N = 144): the
 //                         16 extra output columns are the block's row sums of the
 //                         decoded P, so the softmax threads never add them up
@@ -24,7 +24,10 @@
 //              block b-2 is read from its TMEM slot, brought to the current max
 //              and buffered for the mean restore; epilogue O = (O s_v + the
 //              last, partial group of mean terms) / l.
-// TMEM columns: S0 [0,128), S1 [128,256), E0 [256,272), O [272,400), E1 [400,416).
+// TMEM columns: S0 [0,128), S1 [128,256), E0 [256,272), O [272,400), E1 [400,416),
+// P0 [416,448), P1 [448,480), Q [480,512).  Q and P, the A operands of the two
+// contractions, live in TMEM (four FP8 codes per column), so the tensor core
+// reads only K and V from shared memory.
 // Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
 // drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
 #include <cuda.h>
@@ -48,16 +51,14 @@ constexpr uint32_t kTmemCols = 512;
 // TMEM: S0 [0,128), S1 [128,256), row-sum slot E0 [256,272), O [272,400), E1 [400,416).
 // PV of an even block writes [E0 | O] (B = [ones ; V]), of an odd block [O | E1]
 // (B = [V ; ones]): the 16 extra output columns are the block's row sums.
-constexpr uint32_t kTmemE0 = 256, kTmemO = 272, kTmemE1 = 400;
+constexpr uint32_t kTmemE0 = 256, kTmemO = 272, kTmemE1 = 400, kTmemP0 = 416, kTmemQ = 480;
 
 // shared-memory layout (bytes from a 1024-aligned base)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
+constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOnesBytes = 16 * 128;            // 16 rows of E4M3 1.0
 constexpr uint32_t kVStageBytes = kOnesBytes + kTileBytes + kOnesBytes;   // [ones | V | ones]
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffP = kOffV + kVStages * kVStageBytes;
-constexpr uint32_t kOffMA = kOffP + 2 * kTileBytes;
+constexpr uint32_t kOffMA = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
 constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128] buffered row sums
 constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residual scales
@@ -74,6 +75,7 @@ struct Bars {
 };
 
 struct Params {
+    const uint8_t *q8;
     const float *sq, *sk, *v_scale;
     const uint16_t *v_mean;
     uint16_t *O;
@@ -141,10 +143,10 @@ constexpr uint32_t kBarPair0 = 2;     // + quarter: the two warps of one TMEM la
 constexpr float kLazyTau = 8.0f;      // log2 units: the reference max moves by more than 2^8 only
 
 // P codes of this thread's half row (64 keys) against the reference max m,
-// written as four 16-byte chunks of the 128-byte-swizzled P tile.
+// stored as 16 TMEM columns (four codes per column) of the P buffer at `tp`.
 template <bool kExpcast>
-__device__ __forceinline__ void write_codes(const uint32_t (&S)[64], float c, float m, unsigned char *prow, int row,
-                                            int half) {
+__device__ __forceinline__ void write_codes(const uint32_t (&S)[64], float c, float m, uint32_t tp) {
+    uint32_t w[16];
     if constexpr (kExpcast) {
         const float c8 = __fmul_rn(8.0f, c);
         const float bias = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m));
@@ -152,48 +154,28 @@ __device__ __forceinline__ void write_codes(const uint32_t (&S)[64], float c, fl
         const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
         if (__all_sync(0xffffffffu, fabsf(m) < kExpcastFastMax)) {
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j = ch * 16 + 4 * q;
-                    w[q] = expcast4<false>(pk2(S[j], S[j + 1]), pk2(S[j + 2], S[j + 3]), c8x2, c8x2, bx2, bx2);
-                }
-                *reinterpret_cast<uint4 *>(prow + sw128_offset(row, 4 * half + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            for (int q = 0; q < 16; ++q)
+                w[q] = expcast4<false>(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), c8x2, c8x2, bx2, bx2);
         } else {
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                uint32_t w[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int j = ch * 16 + 4 * q;
-                    w[q] = expcast4<true>(pk2(S[j], S[j + 1]), pk2(S[j + 2], S[j + 3]), c8x2, c8x2, bx2, bx2);
-                }
-                *reinterpret_cast<uint4 *>(prow + sw128_offset(row, 4 * half + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-            }
+            for (int q = 0; q < 16; ++q)
+                w[q] = expcast4<true>(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), c8x2, c8x2, bx2, bx2);
         }
     } else {
         const float negm = -m;
         const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
         const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-            uint32_t w[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int j = ch * 16 + 4 * q;
-                w[q] = expconv4(pk2(S[j], S[j + 1]), pk2(S[j + 2], S[j + 3]), cx2, nx2);
-            }
-            *reinterpret_cast<uint4 *>(prow + sw128_offset(row, 4 * half + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
+        for (int q = 0; q < 16; ++q)
+            w[q] = expconv4(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), cx2, nx2);
     }
+    VCA_TMEM_ST16(tp, w);
 }
 
 template <bool kExpcast>
 __global__ void __launch_bounds__(kThreads, 1)
-    attention_e4m3_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                          const __grid_constant__ CUtensorMap tmV, const Params p) {
+    attention_e4m3_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -221,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = p.N, nb = N / kBlk;
 
     if (threadIdx.x == 0) {
-        mbar_init(B.q_full, 1);
+        mbar_init(B.q_full, 4);   // the four warps that store Q into TMEM
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(B.k_full + s, 1);
             mbar_init(B.k_empty + s, 1);
@@ -263,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 || warp == kVWarp) {
         // ------------------------------------------------------------ producers
-        // warp 0: Q once, then the K ring; warp kVWarp: the V ring.  The rings
+        // warp 0: the K ring; warp kVWarp: the V ring.  The rings
         // are independent, so a K tile is requested as soon as the QK MMA of
         // the tile it replaces is done (not only after that block's PV).
         if (lane == 0) {
@@ -277,11 +259,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(tm);
             int armed[kKStages > kVStages ? kKStages : kVStages];
             for (int s = 0; s < stages; ++s) armed[s] = 0;
-            if (is_k) {
-                tma_prefetch_desc(&tmQ);
-                mbar_expect_tx(B.q_full, kTileBytes);
-                tma_load_2d(smem + kOffQ, &tmQ, B.q_full, 0, bh * N + qtile * kBlk);
-            }
             for (int b = 0; b < nb; ++b) {
                 const int s = b % stages, use = b / stages;
                 if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) break;
@@ -290,7 +267,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 armed[s] = use + 1;
             }
             // every copy this thread issued has landed before the CTA can exit
-            if (is_k) drain_wait(B.q_full, 0, p.limit_ns);
             for (int s = 0; s < stages; ++s)
                 if (armed[s] > 0) drain_wait(full + s, (armed[s] - 1) & 1, p.limit_ns);
         }
@@ -301,7 +277,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             constexpr uint32_t idesc_pv = make_idesc(128, 144, 0, 0);
             constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
             const uint32_t sbase = smem_u32(smem);
-            const uint64_t dq = sdesc_k_sw128(sbase + kOffQ);
             const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
             const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
             const uint32_t tO = tmem + kTmemO;
@@ -314,35 +289,38 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kD / 32; ++kk)
-                    mma_f8f6f4(tmem + sb * 128, dq + 2 * kk, dk + 2 * kk, idesc_qk, kk > 0);
+                    mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
                 tc_commit(B.k_empty + s);
                 tc_commit(B.s_full + sb);
                 return true;
             };
+            // Issue order QK(0), QK(1), PV(0), QK(2), PV(1), QK(3), ...: QK(b)
+            // follows PV(b-2), so the commit that signals S(b) also covers PV(b-2)
+            // and the softmax of block b needs no other wait before it reuses
+            // P buffer b&1 and reads the row-sum slot PV(b-2) wrote.
             bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
             ok = ok && issue_qk(0);
             if (nb > 1) ok = ok && issue_qk(1);
             for (int j = 0; ok && j < nb; ++j) {
-                // QK two blocks ahead, as soon as the softmax has read S(j)
-                if (j + 2 < nb && !issue_qk(j + 2)) break;
                 // PV(j): O (+)= P_j V_j with the block's row sums in the extra 16 columns
                 const int s = j % kVStages, pb = j & 1;
                 if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
                 if (!mbar_wait(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
                 tc_fence_after();
-                const uint64_t dp = sdesc_k_sw128(sbase + kOffP + pb * kTileBytes);
                 const uint32_t vstage = sbase + kOffV + s * kVStageBytes;
                 const uint64_t dv = sdesc_k_sw128(pb == 0 ? vstage : vstage + kOnesBytes);
                 const uint32_t td = tmem + (pb == 0 ? kTmemE0 : kTmemO);
+                const uint32_t tp = tmem + kTmemP0 + 32 * pb;
 #pragma unroll
                 for (int kk = 0; kk < kBlk / 32; ++kk)
-                    mma_f8f6f4(td, dp + 2 * kk, dv + 2 * kk, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    mma_f8f6f4_ts(td, tp + 8 * kk, dv + 2 * kk, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
                 if (flush_after(j)) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
                 }
                 tc_commit(B.v_empty + s);
                 tc_commit(B.pv_done + pb);
+                if (j + 2 < nb && !issue_qk(j + 2)) break;
             }
             tc_commit(B.drain);
             drain_wait(B.drain, 0, p.limit_ns);
@@ -359,7 +337,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
         const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
-        unsigned char *sP = smem + kOffP;
         unsigned char *sMA = smem + kOffMA;
         unsigned char *sMB = smem + kOffMB;
         const float kNegInf = __int_as_float(0xff800000);
@@ -368,19 +345,38 @@ __global__ void __launch_bounds__(kThreads, 1)
         int rs_cnt = 0;
         bool ok = true;
         float sk_next = skh[0];
+        if (half == 0) {
+            // Q tile into TMEM (the A operand of QK): this row's 128 codes, 32 columns
+            const uint4 *qrow = reinterpret_cast<const uint4 *>(
+                p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD);
+            uint32_t qv[32];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const uint4 u = qrow[i];
+                qv[4 * i] = u.x;
+                qv[4 * i + 1] = u.y;
+                qv[4 * i + 2] = u.z;
+                qv[4 * i + 3] = u.w;
+            }
+            VCA_TMEM_ST32(tmem + lane_base + kTmemQ, qv);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.q_full);
+        }
         for (int b = 0; b < nb; ++b) {
             const int sb = b & 1;
             const float sk_b = sk_next;
             if (b + 1 < nb) sk_next = skh[b + 1];
+            // S(b) is ready, and with it PV(b-2): P buffer sb is free and the
+            // row-sum slot of this parity holds block b-2's sums
             bool wok = mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns);
-            // PV(b-2) and its row sums are done (also frees P buffer sb)
-            if (b >= 2) wok = wok && mbar_wait(B.pv_done + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns);
             wok = __all_sync(0xffffffffu, wok) && ok;
             uint32_t S[64];
             uint32_t rs_raw = 0;
             float pm = kNegInf;
             const float c = __fmul_rn(__fmul_rn(sqv, sk_b), p.scale_log2);
-            unsigned char *prow = sP + sb * kTileBytes;
+            const uint32_t tp = tmem + lane_base + kTmemP0 + 32 * sb + 16 * half;
             if (wok) {
                 tc_fence_after();
                 const uint32_t tS = tmem + lane_base + sb * 128 + col0;
@@ -410,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sPM[(sb * 2 + half) * kBlk + row] = pm;
                 // codes against the current reference max, on the bet that this
                 // block does not move it (rewritten below when it does)
-                if (b > 0) write_codes<kExpcast>(S, c, m, prow, row, half);
+                if (b > 0) write_codes<kExpcast>(S, c, m, tp);
             }
             ok = bar_and(wok, pair_bar, 64);
             if (!ok) break;
@@ -423,7 +419,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
                 m = bm;
             }
-            if (__any_sync(0xffffffffu, moved)) write_codes<kExpcast>(S, c, m, prow, row, half);
+            if (__any_sync(0xffffffffu, moved)) {
+                tmem_st_wait();   // the optimistic codes land before they are replaced
+                write_codes<kExpcast>(S, c, m, tp);
+            }
             const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
             if (half == 0) {
                 if (alpha != 1.0f) {
@@ -492,9 +491,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ck)) = use_lo ? lv[ck & 1] : hv[ck & 1];
                 }
                 rs_cnt = 0;
+                fence_proxy_async_smem();   // the mean operands are read by the tensor core
             }
             if (ok) {
-                fence_proxy_async_smem();
+                tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(B.p_full + sb);
@@ -666,11 +666,11 @@ __global__ void selftest_timeout_kernel(int32_t *dev_status, uint64_t limit_ns) 
 }  // namespace
 
 cudaError_t launch_attention(const AttentionArgs &a, cudaStream_t st) {
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mk, mv;
     const uint64_t rows = static_cast<uint64_t>(a.BH) * a.N;
-    if (!make_tile_map(&mq, a.q8, rows) || !make_tile_map(&mk, a.k8, rows) || !make_tile_map(&mv, a.v_res, rows))
-        return cudaErrorInvalidValue;
+    if (!make_tile_map(&mk, a.k8, rows) || !make_tile_map(&mv, a.v_res, rows)) return cudaErrorInvalidValue;
     Params p;
+    p.q8 = a.q8;
     p.sq = a.sq;
     p.sk = a.sk;
     p.v_scale = a.v_scale;
@@ -685,11 +685,11 @@ cudaError_t launch_attention(const AttentionArgs &a, cudaStream_t st) {
     if (a.expcast) {
         e = cudaFuncSetAttribute(attention_e4m3_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attention_e4m3_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+        attention_e4m3_kernel<true><<<grid, kThreads, kSmemBytes, st>>>(mk, mv, p);
     } else {
         e = cudaFuncSetAttribute(attention_e4m3_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        attention_e4m3_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
+        attention_e4m3_kernel<false><<<grid, kThreads, kSmemBytes, st>>>(mk, mv, p);
     }
     return cudaGetLastError();
 }
