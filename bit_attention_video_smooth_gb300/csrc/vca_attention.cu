@@ -41,7 +41,9 @@ namespace {
 
 constexpr int kKStages = 3;               // K tiles in flight (released after their QK MMA)
 constexpr int kVStages = 3;               // V tiles in flight (released after their PV MMA)
-constexpr int kSoftmaxWarps = 8;
+constexpr int kParts = 2;                  // softmax threads per query row (column parts)
+constexpr int kCols = kBlk / kParts;       // S columns per softmax thread
+constexpr int kSoftmaxWarps = 4 * kParts;
 constexpr int kVWarp = 2 + kSoftmaxWarps;  // the V producer
 constexpr int kThreads = 32 * (kVWarp + 1);
 constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
@@ -62,8 +64,8 @@ constexpr uint32_t kOffMA = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
 constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128] buffered row sums
 constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residual scales
-constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][2][128] half-row maxima
-constexpr uint32_t kOffL = kOffPM + 4 * kBlk * 4;           // fp32 [128] final row sums
+constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
+constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
 constexpr uint32_t kOffBar = kOffL + kBlk * 4;
 constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 4 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
@@ -145,8 +147,8 @@ constexpr float kLazyTau = 8.0f;      // log2 units: the reference max moves by 
 // P codes of this thread's half row (64 keys) against the reference max m,
 // stored as 16 TMEM columns (four codes per column) of the P buffer at `tp`.
 template <bool kExpcast>
-__device__ __forceinline__ void write_codes(const uint32_t (&S)[64], float c, float m, uint32_t tp) {
-    uint32_t w[16];
+__device__ __forceinline__ void write_codes(const uint32_t (&S)[kCols], float c, float m, uint32_t tp) {
+    uint32_t w[kCols / 4];
     if constexpr (kExpcast) {
         const float c8 = __fmul_rn(8.0f, c);
         const float bias = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m));
@@ -154,11 +156,11 @@ __device__ __forceinline__ void write_codes(const uint32_t (&S)[64], float c, fl
         const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
         if (__all_sync(0xffffffffu, fabsf(m) < kExpcastFastMax)) {
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
+            for (int q = 0; q < kCols / 4; ++q)
                 w[q] = expcast4<false>(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), c8x2, c8x2, bx2, bx2);
         } else {
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
+            for (int q = 0; q < kCols / 4; ++q)
                 w[q] = expcast4<true>(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), c8x2, c8x2, bx2, bx2);
         }
     } else {
@@ -166,10 +168,16 @@ __device__ __forceinline__ void write_codes(const uint32_t (&S)[64], float c, fl
         const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
         const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
+        for (int q = 0; q < kCols / 4; ++q)
             w[q] = expconv4(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), cx2, nx2);
     }
-    VCA_TMEM_ST16(tp, w);
+    if constexpr (kCols == 64) {
+        VCA_TMEM_ST16(tp, w);
+    } else {
+        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tp), "r"(w[0]),
+                     "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                     : "memory");
+    }
 }
 
 template <bool kExpcast>
@@ -328,11 +336,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax
         const int quarter = warp & 3;                              // TMEM lane quarter
-        const int half = (warp - 2) >> 2;                          // S columns 64*half .. 64*half+63
+        const int half = (warp - 2) >> 2;                          // column part: S columns kCols*half ..
         const int row = quarter * 32 + lane;                       // query row in the tile == TMEM lane
         const uint32_t pair_bar = kBarPair0 + quarter;
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t col0 = 64u * half;
+        const uint32_t col0 = static_cast<uint32_t>(kCols) * half;
         const uint32_t tO = tmem + lane_base + kTmemO + col0;
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
@@ -372,16 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             // row-sum slot of this parity holds block b-2's sums
             bool wok = mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns);
             wok = __all_sync(0xffffffffu, wok) && ok;
-            uint32_t S[64];
+            uint32_t S[kCols];
             uint32_t rs_raw = 0;
             float pm = kNegInf;
             const float c = __fmul_rn(__fmul_rn(sqv, sk_b), p.scale_log2);
-            const uint32_t tp = tmem + lane_base + kTmemP0 + 32 * sb + 16 * half;
+            const uint32_t tp = tmem + lane_base + kTmemP0 + 32 * sb + (kCols / 4) * half;
             if (wok) {
                 tc_fence_after();
                 const uint32_t tS = tmem + lane_base + sb * 128 + col0;
-                VCA_TMEM_LD32(tS + 0, (S + 0));
-                VCA_TMEM_LD32(tS + 32, (S + 32));
+#pragma unroll
+                for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S + 32 * i));
                 // half 0 owns the row-sum slot of this parity: read block b-2's
                 // sum, then clear the slot for PV(b) (PV(0) initialises E0 itself)
                 const uint32_t te = tmem + lane_base + (sb == 0 ? kTmemE0 : kTmemE1);
@@ -400,17 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float a[4] = {__uint_as_float(S[0]), __uint_as_float(S[1]), __uint_as_float(S[2]),
                               __uint_as_float(S[3])};
 #pragma unroll
-                for (int j = 4; j < 64; j += 2)
+                for (int j = 4; j < kCols; j += 2)
                     a[(j >> 1) & 3] = max3(a[(j >> 1) & 3], __uint_as_float(S[j]), __uint_as_float(S[j + 1]));
                 pm = fmaxf(max3(a[0], a[1], a[2]), a[3]);
-                sPM[(sb * 2 + half) * kBlk + row] = pm;
+                sPM[(sb * kParts + half) * kBlk + row] = pm;
                 // codes against the current reference max, on the bet that this
                 // block does not move it (rewritten below when it does)
                 if (b > 0) write_codes<kExpcast>(S, c, m, tp);
             }
-            ok = bar_and(wok, pair_bar, 64);
+            ok = bar_and(wok, pair_bar, 32 * kParts);
             if (!ok) break;
-            const float smax = fmaxf(pm, sPM[(sb * 2 + (half ^ 1)) * kBlk + row]);
+            float smax = pm;
+#pragma unroll
+            for (int q = 1; q < kParts; ++q) smax = fmaxf(smax, sPM[(sb * kParts + ((half + q) % kParts)) * kBlk + row]);
             const float bm = __fmul_rn(smax, c);
             // lazy reference-max update: only when the block's max exceeds it by tau
             const bool moved = bm > __fadd_rn(m, kLazyTau);
@@ -448,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ok) {
                     tc_fence_after();
 #pragma unroll 1
-                    for (int i = 0; i < 2; ++i) {
+                    for (int i = 0; i < kCols / 32; ++i) {
                         uint32_t o[32];
                         VCA_TMEM_LD32(tO + 32 * i, o);
                         tmem_ld_wait();
@@ -469,13 +479,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (half == 0) {
 #pragma unroll
                     for (int i = 0; i < kMeanJ; ++i) split_bf16(sRS[i * kBlk + row], hi[i], lo[i]);
-                } else {
+                } else if (half == 1) {
                     const float inv_sv = 1.0f / sSV[row];
 #pragma unroll
                     for (int i = 0; i < kMeanJ; ++i)
                         split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
                 }
                 unsigned char *dst = half == 0 ? sMA : sMB;
+                if (half < 2) {
                 uint4 hv[2], lv[2];
 #pragma unroll
                 for (int g = 0; g < 2; ++g) {
@@ -489,6 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // A: chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo.   B: chunks 0-3 hi; 4-7 lo.
                     const bool use_lo = (half == 0) ? (((ck >> 1) & 1) != 0) : (ck >= 4);
                     *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ck)) = use_lo ? lv[ck & 1] : hv[ck & 1];
+                }
                 }
                 rs_cnt = 0;
                 fence_proxy_async_smem();   // the mean operands are read by the tensor core
@@ -546,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float inv_l = 1.0f / sL[row];
             uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD + col0;
 #pragma unroll 1
-            for (int i = 0; i < 2; ++i) {
+            for (int i = 0; i < kCols / 32; ++i) {
                 uint32_t o[32];
                 VCA_TMEM_LD32(tO + 32 * i, o);
                 tmem_ld_wait();
