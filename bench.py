@@ -108,9 +108,10 @@ def load_peaks():
         return None
 
 
-def attention_traffic(nb_ratio: float):
-    """DRAM bytes per attention launch from the committed ncu summary, scaled to
-    this workload; None when the kernel source changed since the capture."""
+def attention_traffic(w):
+    """DRAM bytes per attention launch from the committed ncu summary, scaled
+    linearly in B*H*N to this workload; None when the kernel source changed
+    since the capture."""
     path = os.path.join(ROOT, "profiles", "attention_traffic.json")
     src = os.path.join(ROOT, "bit_attention_video_smooth_gb300", "csrc", "vca_attention.cu")
     try:
@@ -118,7 +119,8 @@ def attention_traffic(nb_ratio: float):
         h = hashlib.sha256(open(src, "rb").read()).hexdigest()
         if rec.get("kernel_sha256") != h:
             return None
-        return rec["dram_bytes_per_launch"] * nb_ratio / rec.get("units", 1.0)
+        c = rec["captured_on"]
+        return rec["dram_bytes_per_launch"] * (w.B * w.H * w.N) / (c["B"] * c["H"] * c["N"])
     except (OSError, ValueError, KeyError):
         return None
 
@@ -315,7 +317,7 @@ def run_ours(args, w, ws, rank, local):
         peak = 2.0 * 1700.0
         peak_note = "fallback: 2 x 1.7 PF sustained bf16"
     achieved = w.flops / (t_attn * 1e-3) / 1e12
-    traffic = attention_traffic(1.0)
+    traffic = attention_traffic(w)
     line = {
         "metric": "VC-attention TFLOP/s (group + prep + attention step)", "value": value, "unit": "TFLOP/s",
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,

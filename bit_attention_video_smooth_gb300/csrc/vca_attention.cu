@@ -67,13 +67,14 @@ constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residu
 constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
 constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
 constexpr uint32_t kOffBar = kOffL + kBlk * 4;
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 4 + 1;
+constexpr int kDoneBars = 4;              // 'done' barriers, used round-robin
+constexpr int kNumBars = 1 + kKStages + kVStages + 2 * 2 + kDoneBars + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *pv_done, *drain;
+    uint64_t *q_full, *k_full, *v_full, *s_free, *p_full, *done, *drain;
 };
 
 struct Params {
@@ -86,6 +87,16 @@ struct Params {
     float scale_log2;
     uint64_t limit_ns;
 };
+
+// The MMA thread makes one tcgen05.commit per step: commit #b follows QK(b)
+// and PV(b-2), so its completion means S(b) is ready, K tile b-3's stage and
+// V tile (b-2)'s stage are free and P buffer / row-sum slot b&1 can be reused.
+// Commits go round-robin onto kDoneBars barriers; every waiter is at most one
+// phase behind its barrier (each wait below is for a commit whose successor on
+// the same barrier needs work the waiter has not released yet).
+__device__ __forceinline__ bool wait_done(uint64_t *done, int x, int *abort, uint64_t limit_ns) {
+    return mbar_wait(done + x % kDoneBars, (x / kDoneBars) & 1, abort, limit_ns);
+}
 
 // A mean-restore MMA follows PV(b) when the row sums of blocks b-17 .. b-2 are
 // all buffered (they are read two blocks late).
@@ -191,14 +202,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars B;
     B.q_full = bars;
     B.k_full = bars + 1;
-    B.k_empty = B.k_full + kKStages;
-    B.v_full = B.k_empty + kKStages;
-    B.v_empty = B.v_full + kVStages;
-    B.s_full = B.v_empty + kVStages;
-    B.s_free = B.s_full + 2;
+    B.v_full = B.k_full + kKStages;
+    B.s_free = B.v_full + kVStages;
     B.p_full = B.s_free + 2;
-    B.pv_done = B.p_full + 2;
-    B.drain = B.pv_done + 2;
+    B.done = B.p_full + 2;
+    B.drain = B.done + kDoneBars;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_flag = reinterpret_cast<int *>(smem + kOffMisc + 4);
     float *sRS = reinterpret_cast<float *>(smem + kOffRS);
@@ -212,19 +220,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(B.q_full, 4);   // the four warps that store Q into TMEM
-        for (int s = 0; s < kKStages; ++s) {
-            mbar_init(B.k_full + s, 1);
-            mbar_init(B.k_empty + s, 1);
-        }
-        for (int s = 0; s < kVStages; ++s) {
-            mbar_init(B.v_full + s, 1);
-            mbar_init(B.v_empty + s, 1);
-        }
+        for (int s = 0; s < kKStages; ++s) mbar_init(B.k_full + s, 1);
+        for (int s = 0; s < kVStages; ++s) mbar_init(B.v_full + s, 1);
+        for (int i = 0; i < kDoneBars; ++i) mbar_init(B.done + i, 1);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(B.s_full + i, 1);
             mbar_init(B.s_free + i, kSoftmaxWarps);
             mbar_init(B.p_full + i, kSoftmaxWarps);
-            mbar_init(B.pv_done + i, 1);
         }
         mbar_init(B.drain, 1);
         *abort_flag = 0;
@@ -260,7 +261,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool is_k = (warp == 0);
             const int stages = is_k ? kKStages : kVStages;
             uint64_t *full = is_k ? B.k_full : B.v_full;
-            uint64_t *empty = is_k ? B.k_empty : B.v_empty;
             unsigned char *ring = smem + (is_k ? kOffK : kOffV + kOnesBytes);
             const uint32_t stride = is_k ? kTileBytes : kVStageBytes;
             const void *tm = is_k ? static_cast<const void *>(&tmK) : static_cast<const void *>(&tmV);
@@ -269,7 +269,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < stages; ++s) armed[s] = 0;
             for (int b = 0; b < nb; ++b) {
                 const int s = b % stages, use = b / stages;
-                if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) break;
+                // stage reuse: K tile b-3 was read by QK(b-3) (commit #b-3), V tile
+                // b-3 by PV(b-3) (commit #b-1)
+                if (use > 0 && !wait_done(B.done, is_k ? b - stages : b - stages + 2, abort_flag, p.limit_ns)) break;
                 mbar_expect_tx(full + s, kTileBytes);
                 tma_load_2d(ring + s * stride, tm, full + s, 0, is_k ? bh * N + b * kBlk : (bh * nb + b) * kBlk);
                 armed[s] = use + 1;
@@ -288,47 +290,41 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
             const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
             const uint32_t tO = tmem + kTmemO;
-            // QK(b) -> S[b & 1]; needs K(b) and S[b & 1] released by the softmax of b-2
-            auto issue_qk = [&](int b) -> bool {
-                const int s = b % kKStages, sb = b & 1;
-                if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) return false;
-                if (b >= 2 && !mbar_wait(B.s_free + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns)) return false;
-                tc_fence_after();
-                const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
-#pragma unroll
-                for (int kk = 0; kk < kD / 32; ++kk)
-                    mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
-                tc_commit(B.k_empty + s);
-                tc_commit(B.s_full + sb);
-                return true;
-            };
-            // Issue order QK(0), QK(1), PV(0), QK(2), PV(1), QK(3), ...: QK(b)
-            // follows PV(b-2), so the commit that signals S(b) also covers PV(b-2)
-            // and the softmax of block b needs no other wait before it reuses
-            // P buffer b&1 and reads the row-sum slot PV(b-2) wrote.
+            // step b: PV(b-2) (once P(b-2) is written), then QK(b) (once K(b) has
+            // landed and the softmax has read S(b-2) out of S[b & 1]), then one
+            // commit #b
             bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
-            ok = ok && issue_qk(0);
-            if (nb > 1) ok = ok && issue_qk(1);
-            for (int j = 0; ok && j < nb; ++j) {
-                // PV(j): O (+)= P_j V_j with the block's row sums in the extra 16 columns
-                const int s = j % kVStages, pb = j & 1;
-                if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
-                if (!mbar_wait(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
-                tc_fence_after();
-                const uint32_t vstage = sbase + kOffV + s * kVStageBytes;
-                const uint64_t dv = sdesc_k_sw128(pb == 0 ? vstage : vstage + kOnesBytes);
-                const uint32_t td = tmem + (pb == 0 ? kTmemE0 : kTmemO);
-                const uint32_t tp = tmem + kTmemP0 + 32 * pb;
+            for (int b = 0; ok && b < nb + 2; ++b) {
+                const int j = b - 2;
+                if (j >= 0) {
+                    const int s = j % kVStages, pb = j & 1;
+                    if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
+                    if (!mbar_wait(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
+                    tc_fence_after();
+                    const uint32_t vstage = sbase + kOffV + s * kVStageBytes;
+                    const uint64_t dv = sdesc_k_sw128(pb == 0 ? vstage : vstage + kOnesBytes);
+                    const uint32_t td = tmem + (pb == 0 ? kTmemE0 : kTmemO);
+                    const uint32_t tp = tmem + kTmemP0 + 32 * pb;
+                    // O (+)= P_j V_j with the block's row sums in the extra 16 columns
 #pragma unroll
-                for (int kk = 0; kk < kBlk / 32; ++kk)
-                    mma_f8f6f4_ts(td, tp + 8 * kk, dv + 2 * kk, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                if (flush_after(j)) {
+                    for (int kk = 0; kk < kBlk / 32; ++kk)
+                        mma_f8f6f4_ts(td, tp + 8 * kk, dv + 2 * kk, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                    if (flush_after(j)) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
+                        for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
+                    }
                 }
-                tc_commit(B.v_empty + s);
-                tc_commit(B.pv_done + pb);
-                if (j + 2 < nb && !issue_qk(j + 2)) break;
+                if (b < nb) {
+                    const int s = b % kKStages, sb = b & 1;
+                    if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) break;
+                    if (b >= 2 && !mbar_wait(B.s_free + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns)) break;
+                    tc_fence_after();
+                    const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kD / 32; ++kk)
+                        mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
+                }
+                tc_commit(B.done + b % kDoneBars);
             }
             tc_commit(B.drain);
             drain_wait(B.drain, 0, p.limit_ns);
@@ -378,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (b + 1 < nb) sk_next = skh[b + 1];
             // S(b) is ready, and with it PV(b-2): P buffer sb is free and the
             // row-sum slot of this parity holds block b-2's sums
-            bool wok = mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns);
+            bool wok = wait_done(B.done, b, abort_flag, p.limit_ns);
             wok = __all_sync(0xffffffffu, wok) && ok;
             uint32_t S[kCols];
             uint32_t rs_raw = 0;
@@ -454,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // MMA after it) finished
             if (rescale) {
                 const int jb = b - 1;
-                ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + (jb & 1), (jb >> 1) & 1, abort_flag, p.limit_ns));
+                ok = __all_sync(0xffffffffu, wait_done(B.done, jb + 2, abort_flag, p.limit_ns));
                 if (ok) {
                     tc_fence_after();
 #pragma unroll 1
@@ -517,7 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         if (ok) {
             const int jb = nb - 1;
-            ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + (jb & 1), (jb >> 1) & 1, abort_flag, p.limit_ns));
+            ok = __all_sync(0xffffffffu, wait_done(B.done, jb + 2, abort_flag, p.limit_ns));
         }
         // every softmax warp arrives here, whether it finished or gave up; the
         // epilogue (and its barriers) runs only if all of them finished

@@ -1,0 +1,94 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times (all heads in one launch), checked on outputs the oracle computes one by
+one: whole (b,h) slices of the prep, sampled query rows of the attention, and
+the group on sampled heads.
+
+Workloads: the Wan2.2-14B-shaped video self-attention (B=1, H=40, N=70,656)
+with ExpCast and with the exp path, and the sequence-length sweep at H=40.
+Inputs are drawn on the device from the seeded recipe and copied to the host
+for the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+from bit_attention_video_smooth_gb300 import inputs as I
+
+pytestmark = pytest.mark.gpu
+
+REL_L2 = 1e-3
+MAX_ABS = 4e-3
+
+
+@pytest.fixture(scope="module")
+def V():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_attention_video_smooth_gb300 import vca
+    return vca
+
+
+def _u16(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def _f32(u16):
+    return (np.asarray(u16, np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _check_prep_and_attention(V, orc, w, seed, heads, nrows=48):
+    vmode = V.VCA_V_NVFP4 if w.vmode == "nvfp4" else V.VCA_V_E4M3
+    Q, K, Vv = I.make_qkv(w, seed=seed, device="cuda")
+    perm = I.random_perm(w.BH, w.N, seed=seed + 1, device="cuda")
+    p = V.prep_quant(Q, K, Vv, perm, vmode)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = V.attention(p, w.B, w.H, w.N, expcast=w.expcast, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    Qf, Kf, Vf = (t.view(w.BH, w.N, 128) for t in (Q, K, Vv))
+    rows = I.sample_rows(w.N, nrows, seed=seed).numpy()
+    mode = orc.P_NVFP4 if vmode else (orc.P_EXPCAST if w.expcast else orc.P_EXP)
+    for h in heads:
+        ref = orc.prep(_u16(Qf[h])[None], _u16(Kf[h])[None], _u16(Vf[h])[None], perm[h].cpu().numpy()[None],
+                       vmode=vmode)
+        assert np.array_equal(p.q8[h].cpu().numpy(), ref["q8"][0])
+        assert np.array_equal(p.k8[h].cpu().numpy(), ref["k8"][0])
+        assert np.array_equal(p.sq[h].cpu().numpy(), ref["sq"][0])
+        vr = p.v_res[h].cpu().numpy()
+        assert (vr == ref["v_res"][0]).mean() >= 0.9999
+        O_ref = _f32(orc.attention(ref, mode, rows=rows)[0])
+        got = _f32(_u16(O.view(w.BH, w.N, 128)[h])[rows])
+        rel = np.linalg.norm(got - O_ref) / np.linalg.norm(O_ref)
+        mx = np.abs(got - O_ref).max() / np.abs(O_ref).max()
+        assert rel <= REL_L2 and mx <= MAX_ABS, (h, rel, mx)
+
+
+@pytest.mark.parametrize("name", ["wan", "wan_exp"])
+def test_fullsize_prep_and_attention(V, orc, name):
+    w = I.WORKLOADS[name]
+    _check_prep_and_attention(V, orc, w, seed=31, heads=(0, w.BH - 1))
+
+
+@pytest.mark.parametrize("N", [4096, 16384, 32768, 131072])
+def test_sweep_prep_and_attention(V, orc, N):
+    w = I.with_n(I.WORKLOADS["sweep"], N)
+    _check_prep_and_attention(V, orc, w, seed=41 + N % 97, heads=(w.BH // 2,), nrows=24)
+
+
+def test_fullsize_group_sampled_heads(V, orc):
+    w = I.WORKLOADS["wan"]
+    _, _, Vv = I.make_qkv(w, seed=51, device="cuda")
+    g = V.group(Vv, w.k, w.iters)
+    torch.cuda.synchronize()
+    lab, perm, cnt, cent = (t.cpu().numpy() for t in (g.labels, g.perm, g.counts, g.centroids))
+    Vf = Vv.view(w.BH, w.N, 128)
+    for h in (3, w.BH - 2):
+        assert np.array_equal(perm[h], np.argsort(lab[h], kind="stable"))
+        assert np.array_equal(cnt[h], np.bincount(lab[h], minlength=w.k))
+        v16 = _u16(Vf[h])
+        ref_lab, _, ref_cnt, ref_cent = orc.group(v16[None], w.k, w.iters)
+        agree = (lab[h] == ref_lab[0]).mean()
+        assert agree > 0.99, agree
+        sse_gpu = orc.kmeans_sse(v16, lab[h], cent[h])
+        sse_ref = orc.kmeans_sse(v16, ref_lab[0], ref_cent[0])
+        assert sse_gpu <= sse_ref * 1.005, (sse_gpu, sse_ref)
