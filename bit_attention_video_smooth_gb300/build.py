@@ -14,8 +14,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libvca.so")
-SOURCES = ["vca_api.cu", "vca_group.cu", "vca_prep.cu", "vca_attention.cu", "vca_noalloc.cu"]
-HEADERS = ["vca_device.cuh", "vca_internal.h"]
+SOURCES = ["vca_api.cu", "vca_group.cu", "vca_prep.cu", "vca_attention.cu", "vca_attention_fp4.cu", "vca_noalloc.cu"]
+HEADERS = ["vca_device.cuh", "vca_attention_common.cuh", "vca_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
 

@@ -92,7 +92,6 @@ int vca_attention(const uint8_t *q8, const float *sq, const uint8_t *k8, const f
     if (vmode == VCA_V_NVFP4) {
         if (expcast) return VCA_ERR_UNSUPPORTED;   // no single affine log -> E2M1 code map
         if (!v_sf || !aligned16(v_sf)) return VCA_ERR_INVALID_ARG;
-        return VCA_ERR_UNSUPPORTED;                // 4-bit PV kernel not built yet
     }
     if (softmax_scale <= 0.0f) softmax_scale = static_cast<float>(1.0 / std::sqrt(static_cast<double>(d)));
     vca::AttentionArgs a;
@@ -112,7 +111,8 @@ int vca_attention(const uint8_t *q8, const float *sq, const uint8_t *k8, const f
     a.expcast = expcast;
     a.vmode = vmode;
     a.wait_limit_ns = g_wait_limit_ns;
-    return from_cuda(vca::launch_attention(a, static_cast<cudaStream_t>(stream)));
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    return from_cuda(vmode == VCA_V_NVFP4 ? vca::launch_attention_nvfp4(a, st) : vca::launch_attention(a, st));
 }
 
 int vca_expcast_codes(const float *s_raw, const float *c, const float *m, int64_t n, uint8_t *out, void *stream) {

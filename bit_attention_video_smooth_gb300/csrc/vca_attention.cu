@@ -30,23 +30,19 @@
 // reads only K and V from shared memory.
 // Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
 // drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
-#include <cuda.h>
-
-#include "vca_device.cuh"
+#include "vca_attention_common.cuh"
 #include "vca_internal.h"
 
 namespace vca {
 
 namespace {
 
+using namespace attn;
+
 constexpr int kKStages = 3;               // K tiles in flight (released after their QK MMA)
 constexpr int kVStages = 3;               // V tiles in flight (released after their PV MMA)
-constexpr int kParts = 2;                  // softmax threads per query row (column parts)
-constexpr int kCols = kBlk / kParts;       // S columns per softmax thread
-constexpr int kSoftmaxWarps = 4 * kParts;
 constexpr int kVWarp = 2 + kSoftmaxWarps;  // the V producer
 constexpr int kThreads = 32 * (kVWarp + 1);
-constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
 constexpr int kRsCap = 32;                 // buffered row sums per row (<= 17 in use)
 constexpr uint32_t kTileBytes = kBlk * kD; // one 128 x 128 FP8 tile (16 KB)
 constexpr uint32_t kTmemCols = 512;
@@ -102,30 +98,6 @@ __device__ __forceinline__ bool wait_done(uint64_t *done, int x, int *abort, uin
 // all buffered (they are read two blocks late).
 __host__ __device__ constexpr bool flush_after(int b) { return b >= kMeanJ + 1 && (b % kMeanJ) == 1; }
 
-// Wait ignoring the abort flag (used only to drain work this thread issued).
-__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
-    const uint64_t t0 = globaltimer_ns();
-    while (!mbar_try_wait(bar, parity))
-        if (globaltimer_ns() - t0 > limit_ns) return;
-}
-
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-}
-
-// hi + lo split of x into two bf16 values (x ~= hi + lo to ~16 bits).
-__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
-    hi = __bfloat162float(__float2bfloat16_rn(x));
-    lo = __fsub_rn(x, hi);
-}
-
-__device__ __forceinline__ float max3(float a, float b, float c) {
-    float d;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 // exp2 then E4M3 for four raw scores: p = 2^(fma(S, c, -m)).
 __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_t cx2, uint64_t negmx2) {
     float a[4];
@@ -133,27 +105,6 @@ __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_
     upk2(fma2(s23, cx2, negmx2), a[2], a[3]);
     return e4m3x2(ex2_approx(a[0]), ex2_approx(a[1])) | (e4m3x2(ex2_approx(a[2]), ex2_approx(a[3])) << 16);
 }
-
-// Named barrier that also ANDs a flag over its `count` threads.
-__device__ __forceinline__ bool bar_and(bool v, uint32_t id, uint32_t count) {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.u32 p, %1, 0;\n\t"
-        "bar.red.and.pred q, %2, %3, p;\n\t"
-        "selp.u32 %0, 1, 0, q;\n\t}\n"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-constexpr uint32_t kBarSoftmax = 1;   // all softmax warps (256 threads)
-constexpr uint32_t kBarPair0 = 2;     // + quarter: the two warps of one TMEM lane quarter (64 threads)
-
-constexpr float kLazyTau = 8.0f;      // log2 units: the reference max moves by more than 2^8 only
 
 // P codes of this thread's half row (64 keys) against the reference max m,
 // stored as 16 TMEM columns (four codes per column) of the P buffer at `tp`.
@@ -351,18 +302,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         float sk_next = skh[0];
         if (half == 0) {
             // Q tile into TMEM (the A operand of QK): this row's 128 codes, 32 columns
-            const uint4 *qrow = reinterpret_cast<const uint4 *>(
-                p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD);
-            uint32_t qv[32];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const uint4 u = qrow[i];
-                qv[4 * i] = u.x;
-                qv[4 * i + 1] = u.y;
-                qv[4 * i + 2] = u.z;
-                qv[4 * i + 3] = u.w;
-            }
-            VCA_TMEM_ST32(tmem + lane_base + kTmemQ, qv);
+            load_q_row(p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD,
+                       tmem + lane_base + kTmemQ);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -401,12 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(B.s_free + sb);
-                float a[4] = {__uint_as_float(S[0]), __uint_as_float(S[1]), __uint_as_float(S[2]),
-                              __uint_as_float(S[3])};
-#pragma unroll
-                for (int j = 4; j < kCols; j += 2)
-                    a[(j >> 1) & 3] = max3(a[(j >> 1) & 3], __uint_as_float(S[j]), __uint_as_float(S[j + 1]));
-                pm = fmaxf(max3(a[0], a[1], a[2]), a[3]);
+                pm = row_part_max(S);
                 sPM[(sb * kParts + half) * kBlk + row] = pm;
                 // codes against the current reference max, on the bet that this
                 // block does not move it (rewritten below when it does)
@@ -467,37 +403,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
 
             if (ok && flush_after(b)) {
-                // row sums of blocks b0 .. b0+15 (all at the current max):
-                // A row (query row, half 0):  [rs hi | rs lo | rs hi | rs lo]
-                // B row (channel `row`, half 1): [mu hi | mu hi | mu lo | mu lo], mu = mean / s_v
-                const int b0 = b - kMeanJ - 1;
-                float hi[kMeanJ], lo[kMeanJ];
-                if (half == 0) {
-#pragma unroll
-                    for (int i = 0; i < kMeanJ; ++i) split_bf16(sRS[i * kBlk + row], hi[i], lo[i]);
-                } else if (half == 1) {
-                    const float inv_sv = 1.0f / sSV[row];
-#pragma unroll
-                    for (int i = 0; i < kMeanJ; ++i)
-                        split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
-                }
-                unsigned char *dst = half == 0 ? sMA : sMB;
-                if (half < 2) {
-                uint4 hv[2], lv[2];
-#pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    hv[g] = make_uint4(pack_bf16x2(hi[8 * g + 0], hi[8 * g + 1]), pack_bf16x2(hi[8 * g + 2], hi[8 * g + 3]),
-                                       pack_bf16x2(hi[8 * g + 4], hi[8 * g + 5]), pack_bf16x2(hi[8 * g + 6], hi[8 * g + 7]));
-                    lv[g] = make_uint4(pack_bf16x2(lo[8 * g + 0], lo[8 * g + 1]), pack_bf16x2(lo[8 * g + 2], lo[8 * g + 3]),
-                                       pack_bf16x2(lo[8 * g + 4], lo[8 * g + 5]), pack_bf16x2(lo[8 * g + 6], lo[8 * g + 7]));
-                }
-#pragma unroll
-                for (int ck = 0; ck < 8; ++ck) {
-                    // A: chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo.   B: chunks 0-3 hi; 4-7 lo.
-                    const bool use_lo = (half == 0) ? (((ck >> 1) & 1) != 0) : (ck >= 4);
-                    *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ck)) = use_lo ? lv[ck & 1] : hv[ck & 1];
-                }
-                }
+                // row sums of blocks b0 .. b0+15 (all at the current max)
+                stage_mean_operands(half, row, sRS, vmh, b - kMeanJ - 1, sSV, sMA, sMB);
                 rs_cnt = 0;
                 fence_proxy_async_smem();   // the mean operands are read by the tensor core
             }
@@ -553,29 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             const float inv_l = 1.0f / sL[row];
             uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD + col0;
-#pragma unroll 1
-            for (int i = 0; i < kCols / 32; ++i) {
-                uint32_t o[32];
-                VCA_TMEM_LD32(tO + 32 * i, o);
-                tmem_ld_wait();
-                float acc[32];
-#pragma unroll
-                for (int e = 0; e < 32; ++e) acc[e] = __fmul_rn(__uint_as_float(o[e]), sSV[col0 + 32 * i + e]);
-#pragma unroll 1
-                for (int t = 0; t < rs_cnt; ++t) {
-                    const float r = sRS[t * kBlk + row];
-                    const float *mu = sMu + t * kD + col0 + 32 * i;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) acc[e] = __fmaf_rn(r, mu[e], acc[e]);
-                }
-                uint32_t w[16];
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                    w[e] = pack_bf16x2(__fmul_rn(acc[2 * e], inv_l), __fmul_rn(acc[2 * e + 1], inv_l));
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    reinterpret_cast<uint4 *>(orow + 32 * i)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-            }
+            store_output(tO, sSV, sRS, sMu, rs_cnt, row, static_cast<int>(col0), inv_l, orow);
         }
     }
 
@@ -592,36 +477,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // --------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // --------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
-// 2-D byte matrix [rows][128] with 128 x 128 boxes and the 128-byte swizzle.
-bool make_tile_map(CUtensorMap *map, const void *base, uint64_t rows) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    cuuint64_t dims[2] = {128, rows};
-    cuuint64_t strides[1] = {128};
-    cuuint32_t box[2] = {128, 128};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // ExpCast map alone, for bit-exact tests of the device function.
 // Four elements per thread through the same packed path the attention kernel
 // uses.  The unclipped variant is taken where the attention kernel would take

@@ -1,0 +1,194 @@
+// vca_attention_common.cuh -- pieces both attention kernels (E4M3 residual V
+// with FP8 P, NVFP4 residual V with NVFP4 P) share: the softmax warps' named
+// barriers, the lazy reference-max threshold, the mean-restore operands, the
+// output epilogue and the host-side tensor maps.
+//
+// Mean restore (paper page, "method": the block means come back through the
+// row sums online softmax keeps): O_acc accumulates P (V - mu)/s_v per block;
+// the means come back as sum_b rowsum_b (x) mu_b.  Every kMeanJ key blocks one
+// bf16 MMA adds [rs hi | rs lo | rs hi | rs lo] . [mu' hi | mu' hi | mu' lo | mu' lo]^T
+// (mu' = mu / s_v) to O_acc: the hi/lo bf16 splits keep ~16 bits of both
+// factors and the products are exact in the fp32 accumulator.
+#pragma once
+
+#include <cuda.h>
+
+#include "vca_device.cuh"
+
+namespace vca {
+namespace attn {
+
+constexpr int kParts = 2;                  // softmax threads per query row (column halves)
+constexpr int kCols = kBlk / kParts;       // S columns per softmax thread
+constexpr int kSoftmaxWarps = 4 * kParts;  // two warps per TMEM lane quarter
+constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
+constexpr float kLazyTau = 8.0f;           // log2 units: the reference max moves by more than 2^8 only
+
+constexpr uint32_t kBarSoftmax = 1;        // all softmax warps
+constexpr uint32_t kBarPair0 = 2;          // + quarter: the two warps of one TMEM lane quarter
+
+// Wait ignoring the abort flag (used only to drain work this thread issued).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > limit_ns) return;
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// hi + lo split of x into two bf16 values (x ~= hi + lo to ~16 bits).
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = __fsub_rn(x, hi);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// Largest of a thread's kCols raw scores.
+__device__ __forceinline__ float row_part_max(const uint32_t (&S)[kCols]) {
+    float a[4] = {__uint_as_float(S[0]), __uint_as_float(S[1]), __uint_as_float(S[2]), __uint_as_float(S[3])};
+#pragma unroll
+    for (int j = 4; j < kCols; j += 2)
+        a[(j >> 1) & 3] = max3(a[(j >> 1) & 3], __uint_as_float(S[j]), __uint_as_float(S[j + 1]));
+    return fmaxf(max3(a[0], a[1], a[2]), a[3]);
+}
+
+// Named barrier that also ANDs a flag over its `count` threads.
+__device__ __forceinline__ bool bar_and(bool v, uint32_t id, uint32_t count) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(v)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+__device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Operands of one mean-restore MMA for key blocks b0 .. b0+kMeanJ-1, written
+// by the two threads of query row / channel `row`:
+//   half 0: A row `row` (query row) = [rs hi | rs lo | rs hi | rs lo] from sRS
+//   half 1: B row `row` (channel)   = [mu hi | mu hi | mu lo | mu lo], mu = mean / s_v
+// into the 128-byte-swizzled K-major tiles sMA / sMB.
+__device__ __forceinline__ void stage_mean_operands(int half, int row, const float *sRS, const uint16_t *vmh, int b0,
+                                                    const float *sSV, unsigned char *sMA, unsigned char *sMB) {
+    float hi[kMeanJ], lo[kMeanJ];
+    if (half == 0) {
+#pragma unroll
+        for (int i = 0; i < kMeanJ; ++i) split_bf16(sRS[i * kBlk + row], hi[i], lo[i]);
+    } else {
+        const float inv_sv = 1.0f / sSV[row];
+#pragma unroll
+        for (int i = 0; i < kMeanJ; ++i)
+            split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
+    }
+    unsigned char *dst = half == 0 ? sMA : sMB;
+    uint4 hv[2], lv[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        hv[g] = make_uint4(pack_bf16x2(hi[8 * g + 0], hi[8 * g + 1]), pack_bf16x2(hi[8 * g + 2], hi[8 * g + 3]),
+                           pack_bf16x2(hi[8 * g + 4], hi[8 * g + 5]), pack_bf16x2(hi[8 * g + 6], hi[8 * g + 7]));
+        lv[g] = make_uint4(pack_bf16x2(lo[8 * g + 0], lo[8 * g + 1]), pack_bf16x2(lo[8 * g + 2], lo[8 * g + 3]),
+                           pack_bf16x2(lo[8 * g + 4], lo[8 * g + 5]), pack_bf16x2(lo[8 * g + 6], lo[8 * g + 7]));
+    }
+#pragma unroll
+    for (int ck = 0; ck < 8; ++ck) {
+        // A: chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo.   B: chunks 0-3 hi; 4-7 lo.
+        const bool use_lo = (half == 0) ? (((ck >> 1) & 1) != 0) : (ck >= 4);
+        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ck)) = use_lo ? lv[ck & 1] : hv[ck & 1];
+    }
+}
+
+// O row part = (O_acc s_v + sum_t rs_t mu_t) / l for this thread's kCols
+// channels starting at col0: tO is the TMEM address of those accumulator
+// columns in this thread's lane, sMu the fp32 means [t][128] of the rs_cnt
+// blocks since the last mean MMA, orow the output row at col0.
+__device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, const float *sRS, const float *sMu,
+                                             int rs_cnt, int row, int col0, float inv_l, uint16_t *orow) {
+#pragma unroll 1
+    for (int i = 0; i < kCols / 32; ++i) {
+        uint32_t o[32];
+        VCA_TMEM_LD32(tO + 32 * i, o);
+        tmem_ld_wait();
+        float acc[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) acc[e] = __fmul_rn(__uint_as_float(o[e]), sSV[col0 + 32 * i + e]);
+#pragma unroll 1
+        for (int t = 0; t < rs_cnt; ++t) {
+            const float r = sRS[t * kBlk + row];
+            const float *mu = sMu + t * kD + col0 + 32 * i;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) acc[e] = __fmaf_rn(r, mu[e], acc[e]);
+        }
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__fmul_rn(acc[2 * e], inv_l), __fmul_rn(acc[2 * e + 1], inv_l));
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            reinterpret_cast<uint4 *>(orow + 32 * i)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    }
+}
+
+// Q tile row into TMEM (the A operand of QK): `row`'s 128 E4M3 codes as 32
+// columns at tq (this thread's lane).
+__device__ __forceinline__ void load_q_row(const uint8_t *q8row, uint32_t tq) {
+    const uint4 *qrow = reinterpret_cast<const uint4 *>(q8row);
+    uint32_t qv[32];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 u = qrow[i];
+        qv[4 * i] = u.x;
+        qv[4 * i + 1] = u.y;
+        qv[4 * i + 2] = u.z;
+        qv[4 * i + 3] = u.w;
+    }
+    VCA_TMEM_ST32(tq, qv);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
+}
+
+// 2-D byte matrix [rows][128] with 128 x 128 boxes and the 128-byte swizzle.
+inline bool make_tile_map(CUtensorMap *map, const void *base, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {128, rows};
+    cuuint64_t strides[1] = {128};
+    cuuint32_t box[2] = {128, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace attn
+}  // namespace vca

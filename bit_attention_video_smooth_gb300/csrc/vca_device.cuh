@@ -116,6 +116,15 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// Contiguous global -> shared copy of `bytes` (a multiple of 16; both addresses
+// 16-byte aligned), completing on `bar` through its transaction count.
+__device__ __forceinline__ void bulk_load(void *smem_dst, const void *gmem_src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_u32(smem_dst)),
+                 "l"(reinterpret_cast<uint64_t>(gmem_src)), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
@@ -166,6 +175,19 @@ __device__ __forceinline__ void mma_f8f6f4_ts(uint32_t d_tmem, uint32_t a_tmem, 
         : "memory");
 }
 
+// D(tmem, fp32) (+)= A(tmem) * B(smem)^T, 16-bit operands: A holds M rows in
+// TMEM lanes and K along columns, two 16-bit elements per 32-bit column (the
+// lower K index in the low half).
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
 // D(tmem, fp32) (+)= A(smem) * B(smem)^T, 16-bit operands.
 __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -178,7 +200,7 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
 }
 
 // Instruction descriptor (dense, fp32 accumulator, both operands K-major).
-// atype/btype: kind::f8f6f4 -> 0 = E4M3; kind::f16 -> 1 = BF16.
+// atype/btype: kind::f8f6f4 -> 0 = E4M3; kind::f16 -> 0 = F16, 1 = BF16.
 __host__ __device__ constexpr uint32_t make_idesc(int M, int N, uint32_t atype, uint32_t btype) {
     return (1u << 4)                                   // D format: fp32
            | (atype << 7) | (btype << 10)              // A, B formats

@@ -38,7 +38,8 @@ struct AttentionArgs {
     int expcast, vmode;
     uint64_t wait_limit_ns;
 };
-cudaError_t launch_attention(const AttentionArgs &a, cudaStream_t st);
+cudaError_t launch_attention(const AttentionArgs &a, cudaStream_t st);         // E4M3 residual V
+cudaError_t launch_attention_nvfp4(const AttentionArgs &a, cudaStream_t st);   // NVFP4 residual V and P
 
 cudaError_t launch_expcast_codes(const float *s_raw, const float *c, const float *m, int64_t n, uint8_t *out,
                                  cudaStream_t st);

@@ -138,16 +138,18 @@ int vca_prep_quant_noalloc(const uint16_t *Q, const uint16_t *K, const uint16_t 
  * vca_attention -- non-causal FP8 attention over the prepared operands (paper
  * page, "method": online softmax; ExpCast; the block means come back as one
  * outer product rowsum_b x mean_b per key block, no second pass).  For every
- * query row, key blocks are visited in increasing (permuted) order with the
- * running max m over blocks 0..b; with c = (sq * sk_b) * (softmax_scale *
- * log2 e) and S the raw FP8 product q8 . k8:
+ * query row, key blocks are visited in increasing (permuted) order; with
+ * c = (sq * sk_b) * (softmax_scale * log2 e), S the raw FP8 product q8 . k8
+ * and m the reference max (log2 units), which moves to the block's max
+ * max_j(S_j * c) only when that exceeds m + 8 (the first block always sets it):
  *   expcast = 1:  P = E4M3 byte rne(fma(S, 8c, 55.65 - 8m)), flushed below 8
  *   expcast = 0:  P = E4M3_rne_sat(exp2(fma(S, c, -m)))
- *   NVFP4 mode (expcast must be 0): P is NVFP4 per 16 keys with an E4M3 scale
- *                 E4M3(amax16 / 6)
+ *   NVFP4 mode (expcast must be 0): per 16 keys p = exp2(fma(S, c, -m)),
+ *                 sf = E4M3(amax16 / 6), P = E2M1(p * (1 / sf)) * sf; the V
+ *                 residual decodes to E2M1 * its 16-token E4M3 scale
  *   rowsum_b = sum of the decoded P of block b; l = sum_b rowsum_b
  *   O = (sum_b P_b . v_res_b * v_scale + sum_b rowsum_b (x) v_mean_b) / l
- * with accumulators rescaled by 2^(m_old - m_new) whenever m grows.
+ * with accumulators rescaled by 2^(m_old - m_new) whenever m moves.
  * softmax_scale <= 0 selects 1/sqrt(d).  expcast = 1 with VCA_V_NVFP4 returns
  * VCA_ERR_UNSUPPORTED (NVFP4 has no single affine log-to-code map).
  * dev_status (optional, device int32): set to VCA_ERR_TIMEOUT if a bounded

@@ -4,7 +4,8 @@ one: whole (b,h) slices of the prep, sampled query rows of the attention, and
 the group on sampled heads.
 
 Workloads: the Wan2.2-14B-shaped video self-attention (B=1, H=40, N=70,656)
-with ExpCast and with the exp path, and the sequence-length sweep at H=40.
+with ExpCast and with the exp path, the 4-bit case (NVFP4 V and P, B=2, H=24,
+N=32,768), and the sequence-length sweep at H=40.
 Inputs are drawn on the device from the seeded recipe and copied to the host
 for the oracle.
 """
@@ -56,6 +57,8 @@ def _check_prep_and_attention(V, orc, w, seed, heads, nrows=48):
         assert np.array_equal(p.sq[h].cpu().numpy(), ref["sq"][0])
         vr = p.v_res[h].cpu().numpy()
         assert (vr == ref["v_res"][0]).mean() >= 0.9999
+        if vmode:
+            assert (p.v_sf[h].cpu().numpy() == ref["v_sf"][0]).mean() >= 0.9999
         O_ref = _f32(orc.attention(ref, mode, rows=rows)[0])
         got = _f32(_u16(O.view(w.BH, w.N, 128)[h])[rows])
         rel = np.linalg.norm(got - O_ref) / np.linalg.norm(O_ref)
@@ -63,7 +66,7 @@ def _check_prep_and_attention(V, orc, w, seed, heads, nrows=48):
         assert rel <= REL_L2 and mx <= MAX_ABS, (h, rel, mx)
 
 
-@pytest.mark.parametrize("name", ["wan", "wan_exp"])
+@pytest.mark.parametrize("name", ["wan", "wan_exp", "nvfp4"])
 def test_fullsize_prep_and_attention(V, orc, name):
     w = I.WORKLOADS[name]
     _check_prep_and_attention(V, orc, w, seed=31, heads=(0, w.BH - 1))

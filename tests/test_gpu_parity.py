@@ -173,12 +173,13 @@ def test_prep_nvfp4_parity(V, orc):
 # ---------------------------------------------------------------------------
 # attention
 # ---------------------------------------------------------------------------
-def _prepped_both(V, orc, BH, N, seed):
+def _prepped_both(V, orc, BH, N, seed, vmode=0):
     """Oracle prep of seeded inputs, uploaded as the device operands."""
     q, k, v, perm = _prep_inputs(BH, N, seed)
-    ref = orc.prep(*(I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v)), perm.numpy())
-    p = V.Prepared(_dev(ref["q8"]), _dev(ref["sq"]), _dev(ref["k8"]), _dev(ref["sk"]), _dev(ref["v_res"]), None,
-                   _dev(ref["v_scale"]), _dev(ref["v_mean"], torch.bfloat16), None, V.VCA_V_E4M3)
+    ref = orc.prep(*(I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v)), perm.numpy(), vmode=vmode)
+    v_sf = None if ref["v_sf"] is None else _dev(ref["v_sf"])
+    p = V.Prepared(_dev(ref["q8"]), _dev(ref["sq"]), _dev(ref["k8"]), _dev(ref["sk"]), _dev(ref["v_res"]), v_sf,
+                   _dev(ref["v_scale"]), _dev(ref["v_mean"], torch.bfloat16), None, vmode)
     return ref, p
 
 
@@ -192,6 +193,34 @@ def test_attention_parity_on_oracle_operands(V, orc, expcast, BH, N, seed):
     assert int(status.item()) == 0
     O_ref = orc.attention(ref, orc.P_EXPCAST if expcast else orc.P_EXP)
     rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(BH, N, 128), O_ref)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+# N spans one block, a ragged few, the first mean-restore flush (16 blocks),
+# one block past it (17), and two flushes (32)
+@pytest.mark.parametrize("BH,N,seed", [(1, 128, 21), (3, 384, 22), (2, 2048, 23), (1, 2176, 24), (2, 4096, 25)])
+def test_attention_nvfp4_parity_on_oracle_operands(V, orc, BH, N, seed):
+    ref, p = _prepped_both(V, orc, BH, N, seed, vmode=V.VCA_V_NVFP4)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = V.attention(p, 1, BH, N, expcast=False, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    O_ref = orc.attention(ref, orc.P_NVFP4)
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(BH, N, 128), O_ref)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def test_attention_nvfp4_end_to_end_tiny(V, orc):
+    """GPU NVFP4 prep + attention against oracle NVFP4 prep + attention."""
+    w = I.WORKLOADS["tiny"]
+    q, k, v = I.make_qkv(w, seed=13)
+    perm = I.random_perm(w.BH, w.N, seed=14)
+    ref = orc.prep(*(I.to_u16(t).reshape(w.BH, w.N, 128) for t in (q, k, v)), perm.numpy(), vmode=orc.V_NVFP4)
+    O_ref = orc.attention(ref, orc.P_NVFP4)
+    p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_NVFP4)
+    O = V.attention(p, w.B, w.H, w.N, expcast=False)
+    torch.cuda.synchronize()
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.BH, w.N, 128), O_ref)
     assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
 
 
