@@ -108,21 +108,48 @@ def load_peaks():
         return None
 
 
+# The attention kernel of each V format, and the sources it is built from.
+ATTN_KERNELS = {
+    "e4m3": ("attention_e4m3_kernel", ["vca_attention.cu", "vca_attention_common.cuh", "vca_device.cuh"]),
+    "nvfp4": ("attention_nvfp4_kernel", ["vca_attention_fp4.cu", "vca_attention_common.cuh", "vca_device.cuh"]),
+}
+
+
+def kernel_sources_sha(files):
+    h = hashlib.sha256()
+    for f in files:
+        h.update(open(os.path.join(ROOT, "bit_attention_video_smooth_gb300", "csrc", f), "rb").read())
+    return h.hexdigest()
+
+
 def attention_traffic(w):
     """DRAM bytes per attention launch from the committed ncu summary, scaled
-    linearly in B*H*N to this workload; None when the kernel source changed
+    linearly in B*H*N to this workload; None when the kernel's sources changed
     since the capture."""
-    path = os.path.join(ROOT, "profiles", "attention_traffic.json")
-    src = os.path.join(ROOT, "bit_attention_video_smooth_gb300", "csrc", "vca_attention.cu")
+    name, files = ATTN_KERNELS[w.vmode]
     try:
-        rec = json.load(open(path))
-        h = hashlib.sha256(open(src, "rb").read()).hexdigest()
-        if rec.get("kernel_sha256") != h:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "attention_traffic.json")))[name]
+        if rec.get("sources_sha256") != kernel_sources_sha(files):
             return None
         c = rec["captured_on"]
         return rec["dram_bytes_per_launch"] * (w.B * w.H * w.N) / (c["B"] * c["H"] * c["N"])
     except (OSError, ValueError, KeyError):
         return None
+
+
+def attention_peak(vmode, peaks):
+    """Tensor peak of the attention kernel in TFLOP/s, from the measured
+    sustained cuBLAS bf16 rate b: the E4M3 kernel runs both contractions at the
+    FP8 rate 2b (nominal FP8 / bf16 ratio 4.5 / 2.25); the NVFP4 kernel runs
+    QK (half the FLOPs) at 2b and PV (f16 operands, the other half) at b, so
+    its bound is 1 / (0.5 / 2b + 0.5 / b) = 4b / 3."""
+    if peaks and "bf16_tflops_sustained" in peaks:
+        b, src = peaks["bf16_tflops_sustained"], "measured sustained cuBLAS bf16"
+    else:
+        b, src = 1700.0, "fallback 1.7 PF sustained bf16"
+    if vmode == "e4m3":
+        return 2.0 * b, f"2 x {src} (FP8 / bf16 nominal ratio 4.5 / 2.25)"
+    return 4.0 * b / 3.0, f"4/3 x {src}: QK at the FP8 rate, PV at the f16 rate"
 
 
 # ---------------------------------------------------------------------------
@@ -309,13 +336,7 @@ def run_ours(args, w, ws, rank, local):
         e2e = {"value": ws * w.flops / (ms_e2e * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_e2e,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": hO.numel() * hO.element_size()}
 
-    peaks = load_peaks()
-    if peaks and "bf16_tflops_sustained" in peaks:
-        peak = 2.0 * peaks["bf16_tflops_sustained"]
-        peak_note = "measured: 2 x sustained cuBLAS bf16 (FP8 / bf16 nominal ratio 4.5 / 2.25)"
-    else:
-        peak = 2.0 * 1700.0
-        peak_note = "fallback: 2 x 1.7 PF sustained bf16"
+    peak, peak_note = attention_peak(w.vmode, load_peaks())
     achieved = w.flops / (t_attn * 1e-3) / 1e12
     traffic = attention_traffic(w)
     line = {
@@ -325,12 +346,12 @@ def run_ours(args, w, ws, rank, local):
         "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k, "iters": w.iters,
                    "vmode": w.vmode, "expcast": w.expcast, "parallelism": f"replicas x{ws}",
-                   "l2": "inputs (3 x 724 MB) exceed L2; no flush"},
+                   "l2": f"inputs (3 x {w.BH * w.N * 256 / 1e6:.0f} MB) exceed L2; no flush"},
         "breakdown_ms": {"group": t_group, "prep": t_prep, "attention": t_attn},
         "attention_tflops": achieved,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": traffic, "peak_source": peak_note,
-                     "kernel": "attention_e4m3_kernel"},
+                     "kernel": ATTN_KERNELS[w.vmode][0]},
         "gpu_launches": args.steps * (1 + 2 * w.iters + 1 + 3 + 1),
         "clocks": clocks.summary(),
     }

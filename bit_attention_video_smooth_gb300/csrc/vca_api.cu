@@ -55,14 +55,15 @@ size_t vca_workspace_bytes(int op, int B, int H, int N, int d, int k, int vmode)
 }
 
 int vca_group(const uint16_t *V, int B, int H, int N, int d, int k, int iters, int32_t *labels, int32_t *perm,
-              int32_t *counts, float *centroids, void *ws, size_t ws_bytes, void *stream) {
+              int32_t *counts, float *centroids, void *ws, size_t ws_bytes, int32_t *dev_status, void *stream) {
     if (!shape_ok(B, H, N, d) || k < 1 || k > vca::kMaxK || k > N || iters < 1 || iters > 1000) return VCA_ERR_INVALID_ARG;
     if (!V || !labels || !perm || !aligned16(V) || !aligned16(labels) || !aligned16(perm)) return VCA_ERR_INVALID_ARG;
     if ((counts && !aligned16(counts)) || (centroids && !aligned16(centroids))) return VCA_ERR_INVALID_ARG;
+    if (dev_status && (reinterpret_cast<uintptr_t>(dev_status) & 3u)) return VCA_ERR_INVALID_ARG;
     const size_t need = vca_workspace_bytes(VCA_OP_GROUP, B, H, N, d, k, 0);
     if (!ws || ws_bytes < need || !aligned16(ws)) return VCA_ERR_WORKSPACE;
-    return from_cuda(vca::launch_group(V, B * H, N, k, iters, labels, perm, counts, centroids, ws,
-                                       static_cast<cudaStream_t>(stream)));
+    return from_cuda(vca::launch_group(V, B * H, N, k, iters, labels, perm, counts, centroids, ws, dev_status,
+                                       g_wait_limit_ns, static_cast<cudaStream_t>(stream)));
 }
 
 int vca_prep_quant(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int B, int H, int N,

@@ -34,17 +34,6 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint6
         if (globaltimer_ns() - t0 > limit_ns) return;
 }
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
-}
-
-// hi + lo split of x into two bf16 values (x ~= hi + lo to ~16 bits).
-__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
-    hi = __bfloat162float(__float2bfloat16_rn(x));
-    lo = __fsub_rn(x, hi);
-}
-
 __device__ __forceinline__ float max3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
@@ -160,23 +149,6 @@ __device__ __forceinline__ void load_q_row(const uint8_t *q8row, uint32_t tq) {
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-inline EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(ptr);
-    }
-    return fn;
-}
-
 // 2-D byte matrix [rows][128] with 128 x 128 boxes and the 128-byte swizzle.
 inline bool make_tile_map(CUtensorMap *map, const void *base, uint64_t rows) {
     EncodeTiledFn fn = encode_fn();

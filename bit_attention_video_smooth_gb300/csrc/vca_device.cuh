@@ -5,6 +5,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
@@ -199,11 +200,15 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_
         : "memory");
 }
 
-// Instruction descriptor (dense, fp32 accumulator, both operands K-major).
+// Instruction descriptor (dense, fp32 accumulator, operands K-major unless
+// flagged).
 // atype/btype: kind::f8f6f4 -> 0 = E4M3; kind::f16 -> 0 = F16, 1 = BF16.
-__host__ __device__ constexpr uint32_t make_idesc(int M, int N, uint32_t atype, uint32_t btype) {
+// a_mn / b_mn: the operand is MN-major instead (16-bit types only).
+__host__ __device__ constexpr uint32_t make_idesc(int M, int N, uint32_t atype, uint32_t btype, uint32_t a_mn = 0,
+                                                  uint32_t b_mn = 0) {
     return (1u << 4)                                   // D format: fp32
            | (atype << 7) | (btype << 10)              // A, B formats
+           | (a_mn << 15) | (b_mn << 16)               // A, B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
@@ -219,6 +224,22 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: next 8-row atom
     d |= static_cast<uint64_t>(1) << 46;                    // descriptor version for tcgen05
     d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+    return d;
+}
+
+// Shared-memory matrix descriptor for an MN-major 16-bit operand with the
+// 128-byte swizzle: rows are K indices, each row holds 64 consecutive M (or N)
+// elements (128 bytes), 8-row atoms of 1024 bytes follow each other along K
+// (stride byte offset), and the next 64 M/N elements start `panel_bytes`
+// further on (leading byte offset).  Stepping K by 16 advances the start
+// address by 16 rows (2048 bytes).
+__device__ __forceinline__ uint64_t sdesc_mn_sw128(uint32_t saddr, uint32_t panel_bytes) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);            // start address
+    d |= static_cast<uint64_t>((panel_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset: next MN panel
+    d |= static_cast<uint64_t>(1024 >> 4) << 32;                     // stride byte offset: next 8 K rows
+    d |= static_cast<uint64_t>(1) << 46;                             // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;                             // 128-byte swizzle
     return d;
 }
 
@@ -261,6 +282,19 @@ __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.
 // Number formats
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) { return __uint_as_float(static_cast<uint32_t>(h) << 16); }
+
+// Two fp32 values -> two bf16 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+}
+
+// hi + lo split of x for two bf16 operands: hi = bf16(x), lo = x - hi (exact
+// in fp32; bf16(lo) keeps x to ~16 significant bits).
+__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
+    hi = __bfloat162float(__float2bfloat16_rn(x));
+    lo = __fsub_rn(x, hi);
+}
 
 // Two fp32 values -> two E4M3 bytes (round to nearest even, saturate to 448);
 // `lo` lands in the low byte.
@@ -362,6 +396,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// ---------------------------------------------------------------------------
+// Host: the driver's tensor-map encoder, looked up through the runtime (no
+// link against libcuda)
+// ---------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(ptr);
+    }
+    return fn;
 }
 
 }  // namespace vca

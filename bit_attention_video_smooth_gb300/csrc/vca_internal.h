@@ -13,11 +13,12 @@ constexpr int kMaxK = 128;           // largest supported cluster count
 
 struct GroupWorkspace {
     int nchunk;
-    size_t off_centroids, off_psum, off_pcnt, bytes;
+    size_t off_centroids, off_norm, off_psum, off_pcnt, bytes;
 };
 GroupWorkspace group_workspace_layout(int BH, int N, int k);
 cudaError_t launch_group(const uint16_t *V, int BH, int N, int k, int iters, int32_t *labels, int32_t *perm,
-                         int32_t *counts, float *centroids, void *ws, cudaStream_t st);
+                         int32_t *counts, float *centroids, void *ws, int32_t *dev_status, uint64_t limit_ns,
+                         cudaStream_t st);
 
 struct PrepWorkspace {
     size_t off_amax, off_inv, bytes;

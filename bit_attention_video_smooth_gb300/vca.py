@@ -37,7 +37,7 @@ _SIGS = {
     "vca_status_string": (ctypes.c_char_p, [_I]),
     "vca_version": (_I, []),
     "vca_workspace_bytes": (_SZ, [_I] * 7),
-    "vca_group": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "vca_group": (_I, [_P, _I, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "vca_prep_quant": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "vca_attention": (_I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _F, _I, _I, _P, _P, _P]),
     "vca_expcast_codes": (_I, [_P, _P, _P, _I64, _P, _P]),
@@ -103,10 +103,11 @@ def _u16(t: torch.Tensor) -> torch.Tensor:
 # ---------------------------------------------------------------------------
 def vca_group(V: torch.Tensor, k: int, iters: int, labels: torch.Tensor, perm: torch.Tensor,
               counts: Optional[torch.Tensor], centroids: Optional[torch.Tensor], ws: torch.Tensor,
-              stream=None) -> None:
+              dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
     B, H, N, d = V.shape
     st = _lib.vca_group(_ptr(_u16(V)), B, H, N, d, k, iters, _ptr(labels), _ptr(perm), _ptr(counts),
-                        _ptr(centroids), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+                        _ptr(centroids), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+                        _stream(stream))
     _check(st, "vca_group")
 
 
@@ -207,10 +208,11 @@ def alloc_prep(B, H, N, vmode=VCA_V_E4M3, device="cuda") -> Prepared:
                     torch.empty((BH, nb, d), dtype=torch.bfloat16, device=device), ws, vmode)
 
 
-def group(V: torch.Tensor, k: int, iters: int, out: Optional[Grouped] = None) -> Grouped:
+def group(V: torch.Tensor, k: int, iters: int, out: Optional[Grouped] = None,
+          dev_status: Optional[torch.Tensor] = None) -> Grouped:
     B, H, N, _ = V.shape
     g = out or alloc_group(B, H, N, k, V.device)
-    vca_group(V, k, iters, g.labels, g.perm, g.counts, g.centroids, g.ws)
+    vca_group(V, k, iters, g.labels, g.perm, g.counts, g.centroids, g.ws, dev_status)
     return g
 
 

@@ -82,12 +82,18 @@ size_t vca_workspace_bytes(int op, int B, int H, int N, int d, int k, int vmode)
  *   `iters` rounds of (assign, update); labels are those of the last assign.
  * Outputs: labels [BH][N], perm [BH][N] (tokens ordered by (label, index)),
  * counts [BH][k] (tokens per label), centroids [BH][k][d] (may be NULL).
- * Requires N % 128 == 0, d == 128, 1 <= k <= min(N, 256), iters >= 1,
+ * The distances are taken on the tensor core from bf16 V and the centroids
+ * split into bf16 hi + lo parts (fp32 accumulation): labels equal those of an
+ * exact computation except where two centroids are within ~2^-16 relative of
+ * each other.
+ * Requires N % 128 == 0, d == 128, 1 <= k <= min(N, 128), iters >= 1,
  * ws_bytes >= vca_workspace_bytes(VCA_OP_GROUP, ...).
+ * dev_status (optional, device int32): set to VCA_ERR_TIMEOUT if a bounded
+ * wait inside the kernels ran out; left untouched otherwise.
  */
 int vca_group(const uint16_t *V, int B, int H, int N, int d, int k, int iters,
               int32_t *labels, int32_t *perm, int32_t *counts, float *centroids,
-              void *ws, size_t ws_bytes, void *stream);
+              void *ws, size_t ws_bytes, int32_t *dev_status, void *stream);
 
 /*
  * vca_prep_quant -- the fused V-Smooth prep (paper page, "method": demean each

@@ -68,10 +68,13 @@ def test_invalid_arguments_rejected_without_cuda(lib):
     # ExpCast has no NVFP4 counterpart
     assert lib.vca_attention(*([fake] * 8), 1, 2, 1024, 128, 0.0, 1, 1, fake, None, None) == 2
     lib.vca_group.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
-                              ctypes.c_int, P, P, P, P, P, ctypes.c_size_t, P]
-    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 0, fake, fake, None, None, fake, 1 << 30, None) == 1  # iters
-    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 4, fake, fake, None, None, None, 0, None) == 5          # no ws
-    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 4, fake, fake, None, None, fake, 16, None) == 5         # too small
+                              ctypes.c_int, P, P, P, P, P, ctypes.c_size_t, P, P]
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 0, fake, fake, None, None, fake, 1 << 30, None, None) == 1  # iters
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 200, 4, fake, fake, None, None, fake, 1 << 30, None, None) == 1  # k
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 4, fake, fake, None, None, None, 0, None, None) == 5    # no ws
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 4, fake, fake, None, None, fake, 16, None, None) == 5   # too small
+    assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 4, fake, fake, None, None, fake, 1 << 30, P(0x10002),
+                         None) == 1                                                                       # status
     lib.vca_selftest_timeout.argtypes = [P, ctypes.c_uint64, P]
     assert lib.vca_selftest_timeout(fake, 10, None) == 1
 

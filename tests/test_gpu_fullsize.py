@@ -79,19 +79,48 @@ def test_sweep_prep_and_attention(V, orc, N):
 
 
 def test_fullsize_group_sampled_heads(V, orc):
+    """k-means at the Wan shape on sampled heads.
+
+    One Lloyd round from the fixed initialisation is compared token by token
+    with the oracle: a label may differ only where the token's two candidate
+    centroids are tied to within the rounding of the distance arithmetic.
+    Over the full eight rounds the label sequences of any two implementations
+    drift apart (every near-tie that resolves differently moves a centroid, and
+    the next round's near-ties with it: exact fp32 distances agree with the
+    fp64 oracle on ~97 % of the tokens after eight rounds of this input), so
+    there the test checks what a correct run must satisfy: the permutation and
+    counts follow from the labels, each centroid is the mean of its cluster,
+    and the k-means objective matches the oracle's within 0.1 %."""
     w = I.WORKLOADS["wan"]
     _, _, Vv = I.make_qkv(w, seed=51, device="cuda")
+    g1 = V.group(Vv, w.k, 1)
+    lab1 = g1.labels.cpu().numpy()
     g = V.group(Vv, w.k, w.iters)
     torch.cuda.synchronize()
     lab, perm, cnt, cent = (t.cpu().numpy() for t in (g.labels, g.perm, g.counts, g.centroids))
     Vf = Vv.view(w.BH, w.N, 128)
+    init = ((2 * np.arange(w.k) + 1) * w.N) // (2 * w.k)
     for h in (3, w.BH - 2):
+        v16 = _u16(Vf[h])
+        vf = _f32(v16)
+        # one round: identical labels except at near-ties of the initial centroids
+        ref1, _, _, _ = orc.group(v16[None], w.k, 1)
+        diff = np.nonzero(lab1[h] != ref1[0])[0]
+        assert len(diff) <= 1e-4 * w.N, len(diff)
+        C0 = vf[init]
+        for t in diff:
+            d_gpu = np.sum((vf[t] - C0[lab1[h][t]]) ** 2)
+            d_ref = np.sum((vf[t] - C0[ref1[0][t]]) ** 2)
+            assert abs(d_gpu - d_ref) <= 1e-5 * d_ref, (t, d_gpu, d_ref)
+        # eight rounds: a valid k-means state with the oracle's objective
         assert np.array_equal(perm[h], np.argsort(lab[h], kind="stable"))
         assert np.array_equal(cnt[h], np.bincount(lab[h], minlength=w.k))
-        v16 = _u16(Vf[h])
-        ref_lab, _, ref_cnt, ref_cent = orc.group(v16[None], w.k, w.iters)
-        agree = (lab[h] == ref_lab[0]).mean()
-        assert agree > 0.99, agree
+        scale = np.abs(vf).max()
+        for c in np.nonzero(cnt[h])[0]:
+            mean = vf[lab[h] == c].mean(axis=0)
+            assert np.allclose(cent[h][c], mean, rtol=1e-4, atol=1e-5 * scale), c
+        ref_lab, _, _, ref_cent = orc.group(v16[None], w.k, w.iters)
         sse_gpu = orc.kmeans_sse(v16, lab[h], cent[h])
         sse_ref = orc.kmeans_sse(v16, ref_lab[0], ref_cent[0])
-        assert sse_gpu <= sse_ref * 1.005, (sse_gpu, sse_ref)
+        assert sse_gpu <= sse_ref * 1.001, (sse_gpu, sse_ref)
+        assert (lab[h] == ref_lab[0]).mean() > 0.9
