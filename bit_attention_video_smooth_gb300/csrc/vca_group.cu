@@ -54,7 +54,7 @@ __global__ void __launch_bounds__(kBlk) group_init_kernel(const uint16_t *V, int
 // Shared-memory and TMEM layout of the assign kernel for up to KPAD centroids.
 template <int KPAD>
 struct AssignLayout {
-    static constexpr int kStages = KPAD <= 64 ? 3 : 2;           // V tiles in flight
+    static constexpr int kStages = KPAD <= 64 ? 4 : 2;           // V tiles in flight
     static constexpr int kN = 2 * KPAD;                            // distance MMA N: centroid hi rows, then lo rows
     static constexpr int kDBufs = KPAD <= 64 ? 2 : 1;              // distance accumulators in TMEM
     static constexpr uint32_t kBPanel = kN * 128;                  // one 64-channel panel of the centroid operand

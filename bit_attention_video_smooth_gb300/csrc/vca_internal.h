@@ -8,7 +8,7 @@
 
 namespace vca {
 
-constexpr int kChunkTokens = 2048;   // tokens per CTA in the k-means assign/update kernel
+constexpr int kChunkTokens = 4096;   // tokens per CTA in the k-means assign kernel
 constexpr int kMaxK = 128;           // largest supported cluster count
 
 struct GroupWorkspace {

@@ -89,8 +89,10 @@ def test_e4m3_hardware_conversion_matches_oracle_everywhere(V, orc):
 # ---------------------------------------------------------------------------
 # group: k-means + stable permutation
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("BH,N,k,iters", [(2, 1024, 8, 10), (3, 2 * 2048 + 384, 16, 4), (1, 256, 1, 2),
-                                          (2, 2048, 64, 8), (1, 512, 128, 3)])
+# sizes span one token tile, several 4096-token chunks with a ragged last one,
+# and the cluster counts of both kernel variants (k <= 64, k <= 128)
+@pytest.mark.parametrize("BH,N,k,iters", [(2, 1024, 8, 10), (3, 2 * 4096 + 384, 16, 4), (1, 256, 1, 2),
+                                          (2, 2048, 64, 8), (1, 512, 128, 3), (1, 4096 + 128, 100, 5)])
 def test_group_bit_exact_on_separated_clusters(V, orc, BH, N, k, iters):
     v16 = I.make_separated_v(BH, N, 128, k, seed=BH * 7 + k)
     ref_lab, ref_perm, ref_cnt, ref_cent = orc.group(I.to_u16(v16), k, iters)
