@@ -6,7 +6,7 @@ ExpCast and the mean restore), on the Wan2.2-14B-shaped video self-attention
 workload (B=1, H=40, N=70,656, d=128, k=64, 8 k-means rounds).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload wan|wan_exp|nvfp4|tiny] [--N n]
+                    [--workload wan|wan_exp|nvfp4|tiny] [--N n] [--table]
 
 `value` = attention FLOP (4 B H N^2 d) per second of the whole step, inputs
 resident in device memory; `e2e` = the same with the step's inputs copied from
@@ -42,6 +42,9 @@ def parse():
     ap.add_argument("--N", type=int, default=0, help="override the sequence length")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--table", action="store_true",
+                    help="one line per configuration (tiny, Wan + ExpCast, Wan exp path, NVFP4, the N sweep): "
+                         "each kernel's time against its roofline and the error against exact attention")
     return ap.parse_args()
 
 
@@ -365,8 +368,97 @@ def run_ours(args, w, ws, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------------------
+# per-configuration table: kernels against their rooflines
+# ---------------------------------------------------------------------------
+def group_bytes(w) -> float:
+    """Algorithmic HBM bytes of vca_group: V (bf16) read and labels written once
+    per round, then labels read and the permutation written by the sort."""
+    return w.iters * w.BH * w.N * (w.d * 2 + 4) + w.BH * w.N * 8
+
+
+def prep_bytes(w) -> float:
+    """Algorithmic HBM bytes of vca_prep_quant: Q, K, V (bf16) and the
+    permutation read once; q8, k8 and the V residual (E4M3: 1 byte a value;
+    NVFP4: half a byte plus one E4M3 scale per 16) written once; block means
+    (bf16), Q/K block scales and V scales."""
+    nb = w.N // 128
+    v_res = w.d if w.vmode == "e4m3" else w.d // 2 + w.d // 16
+    v_scale = w.d * 4 if w.vmode == "e4m3" else 4
+    return w.BH * (w.N * (3 * w.d * 2 + 4 + 2 * w.d + v_res) + nb * (w.d * 2 + 8) + v_scale)
+
+
+def table_line(w, peaks, reps: int = 3):
+    import torch
+    from bit_attention_video_smooth_gb300 import inputs as I
+    from bit_attention_video_smooth_gb300 import vca
+
+    vmode = vca.VCA_V_NVFP4 if w.vmode == "nvfp4" else vca.VCA_V_E4M3
+    Q, K, V = I.make_qkv(w, seed=77, device="cuda")
+    g = vca.alloc_group(w.B, w.H, w.N, w.k)
+    p = vca.alloc_prep(w.B, w.H, w.N, vmode)
+    O = torch.empty((w.B, w.H, w.N, 128), dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    stages = {
+        "group": lambda: vca.vca_group(V, w.k, w.iters, g.labels, g.perm, g.counts, g.centroids, g.ws, status),
+        "prep": lambda: vca.vca_prep_quant(Q, K, V, g.perm, vmode, p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf,
+                                           p.v_scale, p.v_mean, p.ws),
+        "attention": lambda: vca.attention(p, w.B, w.H, w.N, expcast=w.expcast, out=O, dev_status=status),
+    }
+    ms = {}
+    for name, fn in stages.items():
+        for _ in range(2):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms[name] = e0.elapsed_time(e1) / reps
+    if int(status.item()) != 0:
+        raise RuntimeError(f"device status {int(status.item())}")
+    # error against exact softmax attention (fp64 on the device) on sampled rows
+    # of the first and last head
+    errs = []
+    rows = I.sample_rows(w.N, 32, seed=5).to("cuda").long()
+    Qf, Kf, Vf = (t.view(w.BH, w.N, 128) for t in (Q, K, V))
+    for h in (0, w.BH - 1):
+        s = (Qf[h, rows].double() @ Kf[h].double().T) / (128 ** 0.5)
+        ref = torch.softmax(s, dim=-1) @ Vf[h].double()
+        got = O.view(w.BH, w.N, 128)[h, rows].double()
+        errs.append(float(torch.linalg.norm(got - ref) / torch.linalg.norm(ref)))
+    peak, _ = attention_peak(w.vmode, peaks)
+    hbm = (peaks or {}).get("hbm_gbs", 6800.0)
+    gb, pb = group_bytes(w), prep_bytes(w)
+    return {
+        "config": w.name, "B": w.B, "H": w.H, "N": w.N, "vmode": w.vmode, "expcast": w.expcast, "k": w.k,
+        "iters": w.iters,
+        "attention_ms": ms["attention"], "attention_tflops": w.flops / ms["attention"] / 1e9,
+        "attention_frac": w.flops / ms["attention"] / 1e9 / peak, "attention_peak_tflops": peak,
+        "group_ms": ms["group"], "group_gbs": gb / ms["group"] / 1e6, "group_frac": gb / ms["group"] / 1e6 / hbm,
+        "prep_ms": ms["prep"], "prep_gbs": pb / ms["prep"] / 1e6, "prep_frac": pb / ms["prep"] / 1e6 / hbm,
+        "hbm_peak_gbs": hbm, "rel_l2_vs_exact_attention": max(errs), "error_rows": "32 sampled rows x 2 heads",
+    }
+
+
+def run_table(args):
+    import torch
+    from bit_attention_video_smooth_gb300 import inputs as I
+    torch.cuda.set_device(0)
+    peaks = load_peaks()
+    cfgs = [I.WORKLOADS["tiny"], I.WORKLOADS["wan"], I.WORKLOADS["wan_exp"], I.WORKLOADS["nvfp4"]]
+    cfgs += [I.with_n(I.WORKLOADS["sweep"], n) for n in (4096, 16384, 32768, 70656, 131072)]
+    for w in cfgs:
+        print(json.dumps(table_line(w, peaks)), flush=True)
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
+    if args.table:
+        run_table(args)
+        return
     from bit_attention_video_smooth_gb300 import inputs as I
     w = I.WORKLOADS[args.workload]
     if args.N:

@@ -325,19 +325,6 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
 // mantissa bits, so the code is the low byte of the sum's bit pattern.
 constexpr float kExpcastOffset = 55.65f;     // 56 + beta, beta = -0.35
 constexpr float kMagic = 12582912.0f;        // 1.5 * 2^23
-__device__ __forceinline__ float expcast_rounded(float s_raw, float c8, float bias) {
-    float x = __fadd_rn(__fmaf_rn(s_raw, c8, bias), kMagic);
-    x = (x >= kMagic + 8.0f) ? x : kMagic;       // NaN and sub-normal-range codes flush to 0
-    return fminf(x, kMagic + 126.0f);
-}
-__device__ __forceinline__ uint32_t expcast_code(float s_raw, float c8, float bias) {
-    return __float_as_uint(expcast_rounded(s_raw, c8, bias)) & 0xFFu;
-}
-// Value of the code held in an expcast_rounded() result: (code + 960) << 20 is
-// the fp32 pattern of a normal E4M3 value; the flushed code decodes to 0.
-__device__ __forceinline__ float expcast_value(float x) {
-    return (x == kMagic) ? 0.0f : __uint_as_float((__float_as_uint(x) << 20) + 0x3C000000u);
-}
 
 // Packed fp32 pairs: two lanes per instruction on sm_100 and later.
 __device__ __forceinline__ uint64_t pk2(uint32_t lo, uint32_t hi) {
@@ -365,8 +352,8 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// Four ExpCast codes packed in one word (byte i = element i), the same
-// arithmetic as expcast_rounded(): per element one fp32 FMA t = fma(s, 8c, bias)
+// Four ExpCast codes packed in one word (byte i = element i): per element one
+// fp32 FMA t = fma(s, 8c, bias)
 // (packed two per instruction), rounding to an integer by adding 1.5 * 2^23,
 // then the clip: codes below 0 (and NaN) become 0 with one max, codes above 126
 // become 126 (kClip), and the bytes 1..7 are zeroed together: a byte b <= 126

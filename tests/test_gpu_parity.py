@@ -11,6 +11,7 @@ import pytest
 import torch
 
 from bit_attention_video_smooth_gb300 import inputs as I
+from cases import LN2_F32, nvfp4_two_block_case, two_block_case
 
 pytestmark = pytest.mark.gpu
 
@@ -224,6 +225,42 @@ def test_attention_nvfp4_end_to_end_tiny(V, orc):
     torch.cuda.synchronize()
     rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(w.BH, w.N, 128), O_ref)
     assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+# The hand-derived two-block examples (worked out in the oracle pins) at the
+# kernels' lazy threshold tau = 8: block 1 (max 4.5) does not move the reference
+# max set by block 0 (max 1).  P0, P1, P129: decoded P of keys 0, 1, 129;
+# rs0, rs1: the blocks' row sums.
+WORKED = {
+    "expcast": dict(P0=1.0, P1=0.625, P129=2.0, rs0=64.625, rs1=77.0),   # key128 code 84 (12.0)
+    "exp": dict(P0=1.0, P1=0.625, P129=2.0, rs0=64.625, rs1=76.0),       # 2^3.5 -> 11.0
+    "nvfp4": dict(P0=1.03125, P1=0.6875, P129=1.875, rs0=66.6875, rs1=84.0),
+}
+
+
+@pytest.mark.parametrize("case", sorted(WORKED))
+def test_attention_worked_example(V, orc, case):
+    """Every query row of the tile is the same row, so all 256 outputs must be
+    the hand-derived values (to the last bf16 place: the kernel forms them in
+    fp32)."""
+    hp = nvfp4_two_block_case(orc) if case == "nvfp4" else two_block_case(orc)
+    vmode = V.VCA_V_NVFP4 if case == "nvfp4" else V.VCA_V_E4M3
+    v_sf = None if hp["v_sf"] is None else _dev(hp["v_sf"])
+    p = V.Prepared(_dev(hp["q8"]), _dev(hp["sq"]), _dev(hp["k8"]), _dev(hp["sk"]), _dev(hp["v_res"]), v_sf,
+                   _dev(hp["v_scale"]), _dev(hp["v_mean"], torch.bfloat16), None, vmode)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = V.attention(p, 1, 1, 256, expcast=(case == "expcast"), softmax_scale=LN2_F32, dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    w = WORKED[case]
+    l = w["rs0"] + w["rs1"]
+    mean = w["rs0"] * 0.5 + w["rs1"] * -0.25
+    want = np.full(128, mean / l)
+    want[0] = (w["P1"] * 2.0 + mean) / l
+    want[1] = (-w["P0"] + w["P129"] + mean) / l
+    got = _f32(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(256, 128)).astype(np.float64)
+    ulp = 2.0 ** (np.floor(np.log2(np.abs(want))) - 7)
+    assert np.all(np.abs(got - want[None, :]) <= ulp[None, :]), (got[0, :3], want[:3])
 
 
 def test_attention_end_to_end_tiny(V, orc):

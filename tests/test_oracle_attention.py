@@ -21,8 +21,8 @@ import pytest
 import torch
 
 from bit_attention_video_smooth_gb300 import inputs as I
+from cases import LN2_F32, nvfp4_two_block_case, two_block_case as _two_block_case
 
-LN2_F32 = float(np.float32(math.log(2.0)))   # softmax scale whose log2(e) multiple is 1.0 in fp32
 
 
 def _f32(u16):
@@ -80,37 +80,6 @@ def test_exact_attention_matches_sdpa_and_is_permutation_invariant(orc):
     np.testing.assert_allclose(Op, O, rtol=1e-12, atol=1e-13)
     rows = np.array([0, 5, 383], np.int32)
     np.testing.assert_allclose(orc.attention_exact(q, k, v, rows=rows), O[:, rows], rtol=0, atol=0)
-
-
-def _two_block_case(orc, third=False):
-    """One (b,h), N = 256 (384 with `third`), d = 128: query row 0 is e4m3 1.0 on channel 0; key j
-    carries a_j on channel 0, so S_raw = a_j; sq = sk = 1 and the softmax scale
-    is fp32(ln 2), making c = 1 and s = S_raw.
-
-    block 0: a = 1.0 (key 0), 0.3125 (key 1), 0 (keys 2..127)
-    block 1: a = 4.5 (key 128), 2.0 (key 129), 0 (keys 130..255)
-    V: residual scale 1; mean 0.5 in block 0, -0.25 in block 1; residual codes
-    2.0 at (key 1, ch 0), -1.0 at (key 0, ch 1), 1.0 at (key 129, ch 1).
-    """
-    N, d = (384 if third else 256), 128
-    code = {v: int(orc.e4m3_encode(np.array([v], np.float32))[0]) for v in (1.0, 0.3125, 4.5, 2.0, -1.0, 12.0)}
-    q8 = np.zeros((1, N, d), np.uint8)
-    q8[0, :, 0] = code[1.0]
-    k8 = np.zeros((1, N, d), np.uint8)
-    k8[0, 0, 0], k8[0, 1, 0], k8[0, 128, 0], k8[0, 129, 0] = code[1.0], code[0.3125], code[4.5], code[2.0]
-    nb = N // 128
-    v_res = np.zeros((1, nb, d, 128), np.uint8)
-    v_res[0, 0, 0, 1] = code[2.0]
-    v_res[0, 0, 1, 0] = code[-1.0]
-    v_res[0, 1, 1, 1] = code[1.0]
-    v_mean = np.zeros((1, nb, d), np.uint16)
-    v_mean[0, 0, :] = orc.bf16_round(0.5)
-    v_mean[0, 1, :] = orc.bf16_round(-0.25)
-    if third:                      # block 2: a = 12 at key 256, mean 1.0
-        k8[0, 256, 0] = code[12.0]
-        v_mean[0, 2, :] = orc.bf16_round(1.0)
-    return {"q8": q8, "sq": np.ones((1, nb), np.float32), "k8": k8, "sk": np.ones((1, nb), np.float32),
-            "v_res": v_res, "v_sf": None, "v_scale": np.ones((1, d), np.float32), "v_mean": v_mean}
 
 
 def test_running_max_schedule_worked_example(orc):
@@ -208,3 +177,44 @@ def test_quantised_p_within_tv_of_exact_p(orc, mode, tol):
     spread = (vh.max(0) - vh.min(0)) / 2
     dev = np.abs(Oq - Oe)[0] / spread[None, :]
     assert dev.max() <= 2 * tol + 2 ** -7
+
+
+def test_nvfp4_worked_example(orc):
+    """NVFP4 P and NVFP4 V on the two-block case (scores as in _two_block_case).
+
+    V: g = 1, every 16-token scale E4M3 1.0; residual E2M1 codes 2.0 at
+    (key 1, ch 0), -1.0 at (key 0, ch 1), 1.0 at (key 129, ch 1); means 0.5 and
+    -0.25.  Per 16 keys: p = 2^(s - m), sf = E4M3(amax / 6),
+    P = E2M1(p / dec(sf)) * dec(sf), worked by hand:
+
+    tau = 8 (m = 1 throughout)
+      block 0, keys 0-15: amax 1 -> sf E4M3(0.16667) = 0.171875 (midpoint to
+               0.15625 is 0.1640625); p/sf: key0 5.818 -> 6 (P 1.03125), key1
+               2^-0.6875 / 0.171875 = 3.611 -> 4 (P 0.6875), p = 0.5 -> 2.909 -> 3
+               (P 0.515625); keys 16-127: amax 0.5 -> sf 0.0859375, 5.818 -> 6
+               (P 0.515625).                                   rowsum0 = 66.6875
+      block 1, keys 128-143: amax 2^3.5 -> sf E4M3(1.8856) = 1.875; key128
+               6.034 -> 6 (saturated, P 11.25), key129 1.0667 -> 1 (P 1.875),
+               0.2667 -> 0.5 (P 0.9375); keys 144-255 as above.  rowsum1 = 84
+    tau = 0 (block 1 moves m to 4.5, alpha = 2^-3.5)
+      block 1, keys 128-143: amax 1 -> sf 0.171875; key128 P 1.03125, key129
+               2^-2.5 / 0.171875 = 1.0285 -> 1 (P 0.171875), 2^-4.5 -> 0.2571 ->
+               0.5 (P 0.0859375); keys 144-255: amax 2^-4.5 -> amax / 6 = 0.0073657
+               lies below E4M3's normal range (2^-6): the subnormal 3.771 * 2^-9
+               rounds to sf = 4 * 2^-9, p / sf = 5.657 -> 6 (P 0.046875).
+                                                               rowsum1 = 7.65625
+    """
+    p = nvfp4_two_block_case(orc)
+    row = np.array([0], np.int32)
+    mean = 66.6875 * 0.5  # block 0's mean term
+    for tau, a, r1, res1 in [(8.0, 1.0, 84.0, (0.0, 1.875)), (0.0, 2.0 ** -3.5, 7.65625, (0.0, 0.171875))]:
+        l = 66.6875 * a + r1
+        ch0 = (a * (0.6875 * 2.0 + mean) + res1[0] + r1 * -0.25) / l
+        ch1 = (a * (1.03125 * -1.0 + mean) + res1[1] + r1 * -0.25) / l
+        rest = (a * mean + r1 * -0.25) / l
+        O, lo = orc.attention(p, orc.P_NVFP4, softmax_scale=LN2_F32, rows=row, return_l=True, tau=tau)
+        got = _f32(O[0, 0])
+        assert lo[0, 0] == pytest.approx(l, rel=1e-15), tau
+        assert got[0] == np.float32(_f32(orc.bf16_round(ch0))), tau
+        assert got[1] == np.float32(_f32(orc.bf16_round(ch1))), tau
+        assert np.all(got[2:] == np.float32(_f32(orc.bf16_round(rest)))), tau
