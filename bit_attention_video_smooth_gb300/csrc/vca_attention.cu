@@ -18,12 +18,15 @@
 //   warps 2-9  softmax: two threads per query row -- the warps w and w+4 share
 //              a TMEM lane quarter and take the S columns 0-63 and 64-127; the
 //              pair exchanges its half-row maxima through shared memory at a
-//              64-thread named barrier.  Running max, O rescale in TMEM when the
-//              max grows, P codes straight to shared memory in the
-//              128-byte-swizzled K-major layout the MMAs read; the row sum of
-//              block b-2 is read from its TMEM slot, brought to the current max
-//              and buffered for the mean restore; epilogue O = (O s_v + the
-//              last, partial group of mean terms) / l.
+//              64-thread named barrier.  Reference max with the lazy threshold
+//              (it moves only when a block's max exceeds it by 8), O rescaled in
+//              TMEM when it moves, P codes stored to TMEM (the A operand of PV);
+//              the row sum of block b-2 is read from its TMEM slot, brought to
+//              the current max and buffered for the mean restore; epilogue
+//              O = (O s_v + the last, partial group of mean terms) / l.
+// The MMA thread waits for P with non-suspending polls (it is on the critical
+// path); it needs no separate signal that S[b&1] is free: every softmax warp
+// reads S(b-2) before it releases P(b-2), which the step has waited for.
 // TMEM columns: S0 [0,128), S1 [128,256), E0 [256,272), O [272,400), E1 [400,416),
 // P0 [416,448), P1 [448,480), Q [480,512).  Q and P, the A operands of the two
 // contractions, live in TMEM (four FP8 codes per column), so the tensor core
@@ -64,13 +67,13 @@ constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][
 constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
 constexpr uint32_t kOffBar = kOffL + kBlk * 4;
 constexpr int kDoneBars = 4;              // 'done' barriers, used round-robin
-constexpr int kNumBars = 1 + kKStages + kVStages + 2 * 2 + kDoneBars + 1;
+constexpr int kNumBars = 1 + kKStages + kVStages + 2 + kDoneBars + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t *q_full, *k_full, *v_full, *s_free, *p_full, *done, *drain;
+    uint64_t *q_full, *k_full, *v_full, *p_full, *done, *drain;
 };
 
 struct Params {
@@ -154,8 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     B.q_full = bars;
     B.k_full = bars + 1;
     B.v_full = B.k_full + kKStages;
-    B.s_free = B.v_full + kVStages;
-    B.p_full = B.s_free + 2;
+    B.p_full = B.v_full + kVStages;
     B.done = B.p_full + 2;
     B.drain = B.done + kDoneBars;
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
@@ -174,10 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < kKStages; ++s) mbar_init(B.k_full + s, 1);
         for (int s = 0; s < kVStages; ++s) mbar_init(B.v_full + s, 1);
         for (int i = 0; i < kDoneBars; ++i) mbar_init(B.done + i, 1);
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(B.s_free + i, kSoftmaxWarps);
-            mbar_init(B.p_full + i, kSoftmaxWarps);
-        }
+        for (int i = 0; i < 2; ++i) mbar_init(B.p_full + i, kSoftmaxWarps);
         mbar_init(B.drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
@@ -250,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (j >= 0) {
                     const int s = j % kVStages, pb = j & 1;
                     if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
-                    if (!mbar_wait(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
+                    if (!mbar_wait_spin(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
                     tc_fence_after();
                     const uint32_t vstage = sbase + kOffV + s * kVStageBytes;
                     const uint64_t dv = sdesc_k_sw128(pb == 0 ? vstage : vstage + kOnesBytes);
@@ -267,8 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (b < nb) {
                     const int s = b % kKStages, sb = b & 1;
+                    // S[b & 1] is free: the softmax read S(b-2) out of it before it
+                    // released P(b-2), which this step has waited for
                     if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) break;
-                    if (b >= 2 && !mbar_wait(B.s_free + sb, ((b >> 1) - 1) & 1, abort_flag, p.limit_ns)) break;
                     tc_fence_after();
                     const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
 #pragma unroll
@@ -333,15 +333,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (half == 0 && b >= 2)
                     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
                 tmem_ld_wait();
-                if (half == 0 && b >= 1) {
+                if (half == 0 && b >= 1)   // completes before P(b) is released
                     asm volatile(
                         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
                         ::"r"(te), "r"(0u) : "memory");
-                    tmem_st_wait();
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B.s_free + sb);
                 pm = row_part_max(S);
                 sPM[(sb * kParts + half) * kBlk + row] = pm;
                 // codes against the current reference max, on the bet that this

@@ -64,6 +64,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of the phase.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // try_wait that may suspend the thread (up to `hint_ns`) until the phase
 // completes, instead of returning at once: waiting warps then stop competing
 // for issue slots with the warps doing the work.
@@ -89,6 +102,26 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, int *a
 #pragma unroll 1
         for (int i = 0; i < 8; ++i)
             if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+        if (*reinterpret_cast<volatile int *>(abort)) return false;
+        if (globaltimer_ns() - t0 > limit_ns) {
+            *reinterpret_cast<volatile int *>(abort) = 1;
+            return false;
+        }
+    }
+}
+
+// mbar_wait for a waiter on the critical path: polls without suspending (a
+// suspended thread resumes some hundreds of cycles after the phase
+// completes), with the same give-up rules.  Each poll is one shared-memory
+// round trip, so the spinning thread takes few issue slots from its
+// neighbours.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t *bar, uint32_t parity, int *abort, uint64_t limit_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+#pragma unroll 1
+        for (int i = 0; i < 64; ++i)
+            if (mbar_test_wait(bar, parity)) return true;
         if (*reinterpret_cast<volatile int *>(abort)) return false;
         if (globaltimer_ns() - t0 > limit_ns) {
             *reinterpret_cast<volatile int *>(abort) = 1;
