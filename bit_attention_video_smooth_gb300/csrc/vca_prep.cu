@@ -83,15 +83,21 @@ __device__ __forceinline__ void quant_qk_block(const uint16_t *__restrict__ X, i
     }
 }
 
-// Gather the block's 128 V rows into shared memory (token-major, padded rows).
-__device__ __forceinline__ void load_v_tile(const uint16_t *__restrict__ V, int64_t head_row0,
-                                            const int32_t *__restrict__ rows, uint16_t *sV) {
+// Gather the block's 128 V rows into shared memory (token-major, padded rows)
+// as asynchronous 16-byte copies (cp.async): all of a thread's copies are in
+// flight at once, and the gather can run while the thread works on something
+// else; cp_async_wait_all() + a barrier before the tile is read.
+__device__ __forceinline__ void load_v_tile_async(const uint16_t *__restrict__ V, int64_t head_row0,
+                                                  const int32_t *__restrict__ rows, uint16_t *sV) {
     for (int u = threadIdx.x; u < kBlk * kD / 8; u += kThreads) {
         const int r = u >> 4, c8 = (u & 15) * 8;
-        *reinterpret_cast<uint4 *>(sV + r * kRowStride + c8) =
-            *reinterpret_cast<const uint4 *>(V + (head_row0 + rows[r]) * kD + c8);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(sV + r * kRowStride + c8)),
+                     "l"(V + (head_row0 + rows[r]) * kD + c8)
+                     : "memory");
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
 }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
 // Error-free transformation: a + b = s + e exactly (Knuth's two-sum).
 __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
@@ -108,36 +114,75 @@ __global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__
                                                               uint8_t *__restrict__ k8, float *__restrict__ sk,
                                                               uint16_t *__restrict__ v_mean,
                                                               float *__restrict__ amax_part) {
-    __shared__ __align__(16) uint16_t sV[kBlk * kRowStride];
+    // the V tile, then 2 x 2 x 128 floats of per-half partial results
+    __shared__ __align__(16) uint16_t sV[kBlk * kRowStride + 4 * kD * 2];
     __shared__ float red[kThreads / 32];
     const int b = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
     const int64_t head_row0 = static_cast<int64_t>(bh) * N;
     const int32_t *rows = perm + head_row0 + static_cast<int64_t>(b) * kBlk;
     const int64_t blk_off = (head_row0 + static_cast<int64_t>(b) * kBlk) * kD;
 
+    // V's gather runs in the background while Q and K are quantised
+    load_v_tile_async(V, head_row0, rows, sV);
     quant_qk_block(Q, head_row0, nullptr, b * kBlk, q8 + blk_off, sq + static_cast<int64_t>(bh) * nb + b, red);
     quant_qk_block(K, head_row0, rows, 0, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b, red);
-
-    load_v_tile(V, head_row0, rows, sV);
+    cp_async_wait_all();
     __syncthreads();
-    const int ch = threadIdx.x;
-    if (ch < kD) {
-        // block mean: compensated fp32 sum (the rounded exact sum), / 128, -> bf16
-        float s = 0.0f, comp = 0.0f;
-        for (int t = 0; t < kBlk; ++t) {
+
+    // Thread (ch, g) takes tokens 64g .. 64g+63 of channel ch: four compensated
+    // (two-sum) partial sums over interleaved tokens, merged in a fixed order;
+    // the two halves meet in shared memory.  The mean is fp32(sum) / 128 ->
+    // bf16, the residual amax max |v - mean| over the block.
+    const int ch = threadIdx.x & (kD - 1), g = threadIdx.x >> 7;
+    const uint16_t *col = sV + (g * 64) * kRowStride + ch;
+    float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f}, c4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+    for (int t = 0; t < 64; t += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
             float e;
-            two_sum(s, bf16_bits_to_f32(sV[t * kRowStride + ch]), s, e);
-            comp = __fadd_rn(comp, e);
+            two_sum(s4[k], bf16_bits_to_f32(col[(t + k) * kRowStride]), s4[k], e);
+            c4[k] = __fadd_rn(c4[k], e);
         }
+    }
+    float sh, ch_c;
+    {
+        float e0, e1, e2;
+        float s01, s23;
+        two_sum(s4[0], s4[1], s01, e0);
+        two_sum(s4[2], s4[3], s23, e1);
+        two_sum(s01, s23, sh, e2);
+        ch_c = __fadd_rn(__fadd_rn(__fadd_rn(c4[0], c4[1]), __fadd_rn(c4[2], c4[3])), __fadd_rn(__fadd_rn(e0, e1), e2));
+    }
+    float *sHalf = reinterpret_cast<float *>(sV + kBlk * kRowStride);   // [2][128] sums, [2][128] compensations
+    __shared__ float sMu[kD];
+    if (g == 1) {
+        sHalf[ch] = sh;
+        sHalf[kD + ch] = ch_c;
+    }
+    __syncthreads();
+    if (g == 0) {
+        float s, e;
+        two_sum(sh, sHalf[ch], s, e);
+        const float comp = __fadd_rn(__fadd_rn(ch_c, sHalf[kD + ch]), e);
         const float mean = __fdiv_rn(__fadd_rn(s, comp), 128.0f);
         const __nv_bfloat16 mu = __float2bfloat16_rn(mean);
-        const float muf = __bfloat162float(mu);
         v_mean[(static_cast<int64_t>(bh) * nb + b) * kD + ch] = __bfloat16_as_ushort(mu);
-        float a = 0.0f;
-        for (int t = 0; t < kBlk; ++t)
-            a = fmaxf(a, fabsf(__fsub_rn(bf16_bits_to_f32(sV[t * kRowStride + ch]), muf)));
-        amax_part[(static_cast<int64_t>(bh) * nb + b) * kD + ch] = a;
+        sMu[ch] = __bfloat162float(mu);
     }
+    __syncthreads();
+    const float muf = sMu[ch];
+    float a4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+    for (int t = 0; t < 64; t += 4) {
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            a4[k] = fmaxf(a4[k], fabsf(__fsub_rn(bf16_bits_to_f32(col[(t + k) * kRowStride]), muf)));
+    }
+    const float a = fmaxf(fmaxf(a4[0], a4[1]), fmaxf(a4[2], a4[3]));
+    if (g == 1) sHalf[ch] = a;
+    __syncthreads();
+    if (g == 0) amax_part[(static_cast<int64_t>(bh) * nb + b) * kD + ch] = fmaxf(a, sHalf[ch]);
 }
 
 // E4M3: per channel a_c -> v_scale = a_c / 448, inv_c = 448 / a_c.
@@ -178,7 +223,8 @@ __global__ void __launch_bounds__(kThreads) prep_vquant_kernel(const uint16_t *_
     const int b = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
     const int64_t head_row0 = static_cast<int64_t>(bh) * N;
     const int32_t *rows = perm + head_row0 + static_cast<int64_t>(b) * kBlk;
-    load_v_tile(V, head_row0, rows, sV);
+    load_v_tile_async(V, head_row0, rows, sV);
+    cp_async_wait_all();
     __syncthreads();
     const int ch = threadIdx.x & (kD - 1);
     const int half = threadIdx.x >> 7;                  // tokens 64*half .. 64*half+63
