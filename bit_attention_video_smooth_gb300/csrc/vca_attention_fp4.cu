@@ -71,7 +71,9 @@ constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128
 constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128]: g for every channel
 constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
 constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
-constexpr uint32_t kOffBar = kOffL + kBlk * 4;
+constexpr uint32_t kOffRcp = kOffL + kBlk * 4;              // fp32 [128]: 1 / dec(E4M3 code), 0 for code 0
+constexpr uint32_t kOffSf2 = kOffRcp + kBlk * 4;            // u32 [128]: dec(E4M3 code) as f16 in both halves
+constexpr uint32_t kOffBar = kOffSf2 + kBlk * 4;
 constexpr int kNumBars = 1 + 2 * kKStages + 2 + kVStages + 2 * kRawStages + 1 + 2 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
@@ -121,8 +123,14 @@ __device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
 // NVFP4 P of this thread's kCols keys against the reference max m: per group
 // of 16 keys p = 2^(fma(S, c, -m)), scale sf = E4M3(amax16 / 6), code =
 // E2M1(p * (1 / dec(sf))), decoded value code * dec(sf) as f16 (exact), two
-// keys per word.
-__device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], float c, float m, uint32_t (&P)[kCols / 2]) {
+// keys per word.  amax16 / 6 is the quotient corrected by one FMA step,
+// q = RN(a r), q' = RN(q + RN(a - 6q) r) with r = RN(1/6): equal to the IEEE
+// quotient for every a in [2^-120, 2^30] (checked exhaustively), and below
+// that both round to the E4M3 code 0.  The reciprocal and the f16 pattern of
+// the scale come from per-CTA tables of the 127 codes (sRcp, sSf2).
+__device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], float c, float m, const float *sRcp,
+                                        const uint32_t *sSf2, uint32_t (&P)[kCols / 2]) {
+    constexpr float kSixth = 1.0f / 6.0f;
     const float negm = -m;
     const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
     const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
@@ -140,9 +148,11 @@ __device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], float c, flo
 #pragma unroll
         for (int j = 4; j < 16; j += 2) a[(j >> 1) & 3] = max3(a[(j >> 1) & 3], pv[j], pv[j + 1]);
         const float amax = fmaxf(max3(a[0], a[1], a[2]), a[3]);
-        const uint32_t sf = e4m3(__fdiv_rn(amax, 6.0f));
-        const float inv = sf != 0u ? __frcp_rn(e4m3_to_f32(sf)) : 0.0f;
-        const uint32_t sf2 = e4m3_f16x2_splat(sf);
+        const float q0 = __fmul_rn(amax, kSixth);
+        const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), kSixth, q0);
+        const uint32_t sf = e4m3x2(q1, 0.0f) & 0xFFu;
+        const float inv = sRcp[sf];
+        const uint32_t sf2 = sSf2[sf];
 #pragma unroll
         for (int q = 0; q < 8; ++q)
             P[8 * g + q] = f16x2_mul(e2m1x2_f16x2(e2m1x2(__fmul_rn(pv[2 * q], inv), __fmul_rn(pv[2 * q + 1], inv))), sf2);
@@ -172,6 +182,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sSV = reinterpret_cast<float *>(smem + kOffSV);
     float *sPM = reinterpret_cast<float *>(smem + kOffPM);
     float *sL = reinterpret_cast<float *>(smem + kOffL);
+    float *sRcp = reinterpret_cast<float *>(smem + kOffRcp);
+    uint32_t *sSf2 = reinterpret_cast<uint32_t *>(smem + kOffSf2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qtile = blockIdx.x, bh = blockIdx.y;
@@ -204,6 +216,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 2 && warp < 6) {
         const int t = threadIdx.x - 64;
         sSV[t] = p.v_scale[bh];
+        // scale tables for the E4M3 codes (127 = NaN is never produced)
+        sRcp[t] = (t == 0 || t == 127) ? 0.0f : __frcp_rn(e4m3_to_f32(static_cast<uint32_t>(t)));
+        sSf2[t] = e4m3_f16x2_splat(static_cast<uint32_t>(t));
         // the rows of f16 1.0 at both ends of every panel
         const uint4 ones = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
         for (int st = 0; st < kVStages; ++st)
@@ -413,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = bm;
             }
             uint32_t P[kCols / 2];
-            nvfp4_p(S, c, m, P);
+            nvfp4_p(S, c, m, sRcp, sSf2, P);
             // PV(b-1) is done: the P buffer and O are free, block b-1's row sums
             // are in their slot
             if (b >= 1) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + ((b - 1) & 1), ((b - 1) >> 1) & 1, abort_flag,
