@@ -357,8 +357,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = bm;
             }
             if (__any_sync(0xffffffffu, moved)) {
+                // S(b) is still in TMEM (S[b&1] is rewritten only after P(b) is
+                // released): reload it rather than keep 64 registers live
+                // through the code computation for this rare path
                 tmem_st_wait();   // the optimistic codes land before they are replaced
-                write_codes<kExpcast>(S, c, m, tp);
+                uint32_t S2[kCols];
+                const uint32_t tS = tmem + lane_base + sb * 128 + col0;
+#pragma unroll
+                for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S2 + 32 * i));
+                tmem_ld_wait();
+                write_codes<kExpcast>(S2, c, m, tp);
             }
             const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
             if (half == 0) {
