@@ -338,19 +338,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
                         ::"r"(te), "r"(0u) : "memory");
                 pm = row_part_max(S);
-                sPM[(sb * kParts + half) * kBlk + row] = pm;
                 // codes against the current reference max, on the bet that this
                 // block does not move it (rewritten below when it does)
                 if (b > 0) write_codes<kExpcast>(S, c, m, tp);
             }
-            ok = bar_and(wok, pair_bar, 32 * kParts);
-            if (!ok) break;
-            float smax = pm;
+            // Lazy reference-max update: only when the block's max exceeds m by
+            // tau.  The block max moves m exactly when one part's max does
+            // (scaling by c >= 0 is monotone), so the common case takes one pair
+            // barrier: every thread of the row finished its wait and no part
+            // moves m.  Otherwise the parts exchange their maxima.
+            const float lim = __fadd_rn(m, kLazyTau);
+            const bool quiet = bar_and(wok && !(__fmul_rn(pm, c) > lim), pair_bar, 32 * kParts);
+            float bm = kNegInf;
+            bool moved = false;
+            if (!quiet) {
+                sPM[(sb * kParts + half) * kBlk + row] = pm;
+                ok = bar_and(wok, pair_bar, 32 * kParts);
+                if (!ok) break;
+                float smax = pm;
 #pragma unroll
-            for (int q = 1; q < kParts; ++q) smax = fmaxf(smax, sPM[(sb * kParts + ((half + q) % kParts)) * kBlk + row]);
-            const float bm = __fmul_rn(smax, c);
-            // lazy reference-max update: only when the block's max exceeds it by tau
-            const bool moved = bm > __fadd_rn(m, kLazyTau);
+                for (int q = 1; q < kParts; ++q)
+                    smax = fmaxf(smax, sPM[(sb * kParts + ((half + q) % kParts)) * kBlk + row]);
+                bm = __fmul_rn(smax, c);
+                moved = bm > lim;
+            }
             float alpha = 1.0f;
             if (moved) {
                 if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
