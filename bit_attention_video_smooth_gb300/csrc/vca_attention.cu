@@ -349,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // moves m.  Otherwise the parts exchange their maxima.
             const float lim = __fadd_rn(m, kLazyTau);
             const bool quiet = bar_and(wok && !(__fmul_rn(pm, c) > lim), pair_bar, 32 * kParts);
-            float bm = kNegInf;
-            bool moved = false;
+            float alpha = 1.0f;
+            bool rescale = false;
             if (!quiet) {
                 sPM[(sb * kParts + half) * kBlk + row] = pm;
                 ok = bar_and(wok, pair_bar, 32 * kParts);
@@ -359,40 +359,37 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int q = 1; q < kParts; ++q)
                     smax = fmaxf(smax, sPM[(sb * kParts + ((half + q) % kParts)) * kBlk + row]);
-                bm = __fmul_rn(smax, c);
-                moved = bm > lim;
-            }
-            float alpha = 1.0f;
-            if (moved) {
-                if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
-                m = bm;
-            }
-            if (__any_sync(0xffffffffu, moved)) {
-                // S(b) is still in TMEM (S[b&1] is rewritten only after P(b) is
-                // released): reload it rather than keep 64 registers live
-                // through the code computation for this rare path
-                tmem_st_wait();   // the optimistic codes land before they are replaced
-                uint32_t S2[kCols];
-                const uint32_t tS = tmem + lane_base + sb * 128 + col0;
+                const float bm = __fmul_rn(smax, c);
+                const bool moved = bm > lim;
+                if (moved) {
+                    if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
+                    m = bm;
+                }
+                if (__any_sync(0xffffffffu, moved)) {
+                    // S(b) is still in TMEM (S[b&1] is rewritten only after P(b) is
+                    // released): reload it rather than keep 64 registers live
+                    // through the code computation for this rare path
+                    tmem_st_wait();   // the optimistic codes land before they are replaced
+                    uint32_t S2[kCols];
+                    const uint32_t tS = tmem + lane_base + sb * 128 + col0;
 #pragma unroll
-                for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S2 + 32 * i));
-                tmem_ld_wait();
-                write_codes<kExpcast>(S2, c, m, tp);
-            }
-            const bool rescale = __any_sync(0xffffffffu, alpha != 1.0f);
-            if (half == 0) {
-                if (alpha != 1.0f) {
+                    for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S2 + 32 * i));
+                    tmem_ld_wait();
+                    write_codes<kExpcast>(S2, c, m, tp);
+                }
+                rescale = __any_sync(0xffffffffu, alpha != 1.0f);
+                if (half == 0 && alpha != 1.0f) {
                     l = __fmul_rn(l, alpha);
 #pragma unroll 1
                     for (int i = 0; i < rs_cnt; ++i) sRS[i * kBlk + row] = __fmul_rn(sRS[i * kBlk + row], alpha);
                 }
-                if (b >= 2) {
-                    // row sum of block b-2, taken against that block's max: bring it to m
-                    float rs = __uint_as_float(rs_raw);
-                    if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
-                    l = __fadd_rn(l, rs);
-                    sRS[rs_cnt * kBlk + row] = rs;
-                }
+            }
+            if (half == 0 && b >= 2) {
+                // row sum of block b-2, taken against that block's max: bring it to m
+                float rs = __uint_as_float(rs_raw);
+                if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
+                l = __fadd_rn(l, rs);
+                sRS[rs_cnt * kBlk + row] = rs;
             }
             if (b >= 2) ++rs_cnt;
 
