@@ -428,6 +428,16 @@ def table_line(w, peaks, reps: int = 3):
         ref = torch.softmax(s, dim=-1) @ Vf[h].double()
         got = O.view(w.BH, w.N, 128)[h, rows].double()
         errs.append(float(torch.linalg.norm(got - ref) / torch.linalg.norm(ref)))
+    # V-Smooth diagnostic: the share of V's energy that the 128-token block
+    # means take out, blocks in cluster (permuted) order vs sequence order
+    removed = {"sorted": [], "sequence": []}
+    for h in (0, w.BH - 1):
+        v = Vf[h].double()
+        total = float((v * v).sum())
+        for key, order in (("sorted", g.perm[h].long()), ("sequence", None)):
+            vb = (v if order is None else v[order]).view(w.N // 128, 128, 128)
+            res = vb - vb.mean(dim=1, keepdim=True)
+            removed[key].append(1.0 - float((res * res).sum()) / total)
     peak, _ = attention_peak(w.vmode, peaks)
     hbm = (peaks or {}).get("hbm_gbs", 6800.0)
     gb, pb = group_bytes(w), prep_bytes(w)
@@ -439,6 +449,7 @@ def table_line(w, peaks, reps: int = 3):
         "group_ms": ms["group"], "group_gbs": gb / ms["group"] / 1e6, "group_frac": gb / ms["group"] / 1e6 / hbm,
         "prep_ms": ms["prep"], "prep_gbs": pb / ms["prep"] / 1e6, "prep_frac": pb / ms["prep"] / 1e6 / hbm,
         "hbm_peak_gbs": hbm, "rel_l2_vs_exact_attention": max(errs), "error_rows": "32 sampled rows x 2 heads",
+        "energy_removed_by_block_means": {k: statistics.mean(v) for k, v in removed.items()},
     }
 
 
