@@ -8,13 +8,15 @@
 // blocks of that head in increasing (permuted) order.  Warp roles:
 //   warp 0     TMA producer: K tiles into a 3-stage ring
 //   warp 10    TMA producer: V-residual tiles into a 3-stage ring
-//   warp 1     TMEM owner and MMA issuer (one thread):
-//                S[b&1] = Q8 K8_b^T                 (kind::f8f6f4, N = 128), issued
-//                         right after PV(b-2)
+//   warp 11    QK issuer (one thread): S[b&1] = Q8 K8_b^T (kind::f8f6f4,
+//              N = 128) once K(b) has landed and P(b-2) has been released
+//   warp 1     TMEM owner and PV issuer (one thread):
 //                [E | O] += P_b [ones ; V8_b]       (kind::f8f6f4, N = 144): the
 //                         16 extra output columns are the block's row sums of the
 //                         decoded P, so the softmax threads never add them up
 //              and every 16 key blocks O += [rowsum hi|lo] [mean/s_v hi|lo]^T (bf16).
+//              Two issuing threads keep each one's serial work (barrier
+//              checks, MMA issue, commits) off the other's critical path.
 //   warps 2-9  softmax: two threads per query row -- the warps w and w+4 share
 //              a TMEM lane quarter and take the S columns 0-63 and 64-127; the
 //              pair exchanges its half-row maxima through shared memory at a
@@ -24,9 +26,9 @@
 //              the row sum of block b-2 is read from its TMEM slot, brought to
 //              the current max and buffered for the mean restore; epilogue
 //              O = (O s_v + the last, partial group of mean terms) / l.
-// The MMA thread waits for P with non-suspending polls (it is on the critical
-// path); it needs no separate signal that S[b&1] is free: every softmax warp
-// reads S(b-2) before it releases P(b-2), which the step has waited for.
+// The issuing threads wait for P with non-suspending polls (they are on the
+// critical path); S[b&1] needs no signal of its own: every softmax warp reads
+// S(b-2) before it releases P(b-2), which the QK thread waits for.
 // TMEM columns: S0 [0,128), S1 [128,256), E0 [256,272), O [272,400), E1 [400,416),
 // P0 [416,448), P1 [448,480), Q [480,512).  Q and P, the A operands of the two
 // contractions, live in TMEM (four FP8 codes per column), so the tensor core
@@ -45,7 +47,8 @@ using namespace attn;
 constexpr int kKStages = 3;               // K tiles in flight (released after their QK MMA)
 constexpr int kVStages = 3;               // V tiles in flight (released after their PV MMA)
 constexpr int kVWarp = 2 + kSoftmaxWarps;  // the V producer
-constexpr int kThreads = 32 * (kVWarp + 1);
+constexpr int kQKWarp = kVWarp + 1;        // the QK issuer (the PV issuer is warp 1)
+constexpr int kThreads = 32 * (kQKWarp + 1);
 constexpr int kRsCap = 32;                 // buffered row sums per row (<= 17 in use)
 constexpr uint32_t kTileBytes = kBlk * kD; // one 128 x 128 FP8 tile (16 KB)
 constexpr uint32_t kTmemCols = 512;
@@ -66,14 +69,13 @@ constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residu
 constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
 constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
 constexpr uint32_t kOffBar = kOffL + kBlk * 4;
-constexpr int kDoneBars = 4;              // 'done' barriers, used round-robin
-constexpr int kNumBars = 1 + kKStages + kVStages + 2 + kDoneBars + 1;
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t *q_full, *k_full, *v_full, *p_full, *done, *drain;
+    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *p_full, *s_ready, *drain;
 };
 
 struct Params {
@@ -87,14 +89,15 @@ struct Params {
     uint64_t limit_ns;
 };
 
-// The MMA thread makes one tcgen05.commit per step: commit #b follows QK(b)
-// and PV(b-2), so its completion means S(b) is ready, K tile b-3's stage and
-// V tile (b-2)'s stage are free and P buffer / row-sum slot b&1 can be reused.
-// Commits go round-robin onto kDoneBars barriers; every waiter is at most one
-// phase behind its barrier (each wait below is for a commit whose successor on
-// the same barrier needs work the waiter has not released yet).
-__device__ __forceinline__ bool wait_done(uint64_t *done, int x, int *abort, uint64_t limit_ns) {
-    return mbar_wait(done + x % kDoneBars, (x / kDoneBars) & 1, abort, limit_ns);
+// Two threads issue the MMAs: the QK thread (S(b) = Q K_b^T) and the PV thread
+// (O += P_j V_j and the mean-restore MMAs).  The softmax of block b waits on
+// s_ready[b & 1], whose phase completes on two tcgen05.commit arrivals: the QK
+// thread's after QK(b) (S(b) is in TMEM) and the PV thread's after PV(b-2)
+// (P buffer and row-sum slot b & 1 are free, and the slot holds block b-2's
+// sums).  Every waiter is at most one phase behind: the next phase of
+// s_ready[b & 1] needs PV(b), which needs the softmax's P(b).
+__device__ __forceinline__ bool wait_s_ready(const Bars &B, int b, int *abort, uint64_t limit_ns) {
+    return mbar_wait(B.s_ready + (b & 1), (b >> 1) & 1, abort, limit_ns);
 }
 
 // A mean-restore MMA follows PV(b) when the row sums of blocks b-17 .. b-2 are
@@ -156,10 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     Bars B;
     B.q_full = bars;
     B.k_full = bars + 1;
-    B.v_full = B.k_full + kKStages;
-    B.p_full = B.v_full + kVStages;
-    B.done = B.p_full + 2;
-    B.drain = B.done + kDoneBars;
+    B.k_empty = B.k_full + kKStages;
+    B.v_full = B.k_empty + kKStages;
+    B.v_empty = B.v_full + kVStages;
+    B.p_full = B.v_empty + kVStages;
+    B.s_ready = B.p_full + 2;
+    B.drain = B.s_ready + 2;   // [0]: QK thread, [1]: PV thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_flag = reinterpret_cast<int *>(smem + kOffMisc + 4);
     float *sRS = reinterpret_cast<float *>(smem + kOffRS);
@@ -173,11 +178,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(B.q_full, 4);   // the four warps that store Q into TMEM
-        for (int s = 0; s < kKStages; ++s) mbar_init(B.k_full + s, 1);
-        for (int s = 0; s < kVStages; ++s) mbar_init(B.v_full + s, 1);
-        for (int i = 0; i < kDoneBars; ++i) mbar_init(B.done + i, 1);
-        for (int i = 0; i < 2; ++i) mbar_init(B.p_full + i, kSoftmaxWarps);
-        mbar_init(B.drain, 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(B.k_full + s, 1);
+            mbar_init(B.k_empty + s, 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(B.v_full + s, 1);
+            mbar_init(B.v_empty + s, 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(B.p_full + i, kSoftmaxWarps);
+            mbar_init(B.s_ready + i, 2);   // QK(b) and PV(b-2)
+            mbar_init(B.drain + i, 1);
+        }
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -204,13 +217,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0 || warp == kVWarp) {
         // ------------------------------------------------------------ producers
-        // warp 0: the K ring; warp kVWarp: the V ring.  The rings
-        // are independent, so a K tile is requested as soon as the QK MMA of
-        // the tile it replaces is done (not only after that block's PV).
+        // warp 0: the K ring; warp kVWarp: the V ring.  A stage is refilled
+        // as soon as the MMA that read it has finished (the issuing thread's
+        // commit onto k_empty / v_empty).
         if (lane == 0) {
             const bool is_k = (warp == 0);
             const int stages = is_k ? kKStages : kVStages;
             uint64_t *full = is_k ? B.k_full : B.v_full;
+            uint64_t *empty = is_k ? B.k_empty : B.v_empty;
             unsigned char *ring = smem + (is_k ? kOffK : kOffV + kOnesBytes);
             const uint32_t stride = is_k ? kTileBytes : kVStageBytes;
             const void *tm = is_k ? static_cast<const void *>(&tmK) : static_cast<const void *>(&tmV);
@@ -219,9 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < stages; ++s) armed[s] = 0;
             for (int b = 0; b < nb; ++b) {
                 const int s = b % stages, use = b / stages;
-                // stage reuse: K tile b-3 was read by QK(b-3) (commit #b-3), V tile
-                // b-3 by PV(b-3) (commit #b-1)
-                if (use > 0 && !wait_done(B.done, is_k ? b - stages : b - stages + 2, abort_flag, p.limit_ns)) break;
+                if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) break;
                 mbar_expect_tx(full + s, kTileBytes);
                 tma_load_2d(ring + s * stride, tm, full + s, 0, is_k ? bh * N + b * kBlk : (bh * nb + b) * kBlk);
                 armed[s] = use + 1;
@@ -230,55 +242,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < stages; ++s)
                 if (armed[s] > 0) drain_wait(full + s, (armed[s] - 1) & 1, p.limit_ns);
         }
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == kQKWarp) {
+        // ------------------------------------------------------------ QK issuer
+        // QK(b) into S[b & 1] once K(b) has landed and the softmax has released
+        // P(b-2) (it reads S(b-2) out of S[b & 1] before that); then commits
+        // for the K stage and for s_ready.  Steps nb and nb+1 issue no MMA but
+        // still wait for P(b-2) and commit, so that the last two phases of
+        // s_ready (the epilogue waits for them) complete, each only after the
+        // phase before it on the same barrier.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc(128, 128, 0, 0);
-            constexpr uint32_t idesc_pv = make_idesc(128, 144, 0, 0);
-            constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
             const uint32_t sbase = smem_u32(smem);
-            const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
-            const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
-            const uint32_t tO = tmem + kTmemO;
-            // step b: PV(b-2) (once P(b-2) is written), then QK(b) (once K(b) has
-            // landed and the softmax has read S(b-2) out of S[b & 1]), then one
-            // commit #b
             bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
             for (int b = 0; ok && b < nb + 2; ++b) {
-                const int j = b - 2;
-                if (j >= 0) {
-                    const int s = j % kVStages, pb = j & 1;
-                    if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
-                    if (!mbar_wait_spin(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
-                    tc_fence_after();
-                    const uint32_t vstage = sbase + kOffV + s * kVStageBytes;
-                    const uint64_t dv = sdesc_k_sw128(pb == 0 ? vstage : vstage + kOnesBytes);
-                    const uint32_t td = tmem + (pb == 0 ? kTmemE0 : kTmemO);
-                    const uint32_t tp = tmem + kTmemP0 + 32 * pb;
-                    // O (+)= P_j V_j with the block's row sums in the extra 16 columns
-#pragma unroll
-                    for (int kk = 0; kk < kBlk / 32; ++kk)
-                        mma_f8f6f4_ts(td, tp + 8 * kk, dv + 2 * kk, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                    if (flush_after(j)) {
-#pragma unroll
-                        for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
-                    }
-                }
+                if (b >= 2 && !mbar_wait_spin(B.p_full + (b & 1), ((b - 2) >> 1) & 1, abort_flag, p.limit_ns)) break;
                 if (b < nb) {
                     const int s = b % kKStages, sb = b & 1;
-                    // S[b & 1] is free: the softmax read S(b-2) out of it before it
-                    // released P(b-2), which this step has waited for
                     if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) break;
                     tc_fence_after();
                     const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
 #pragma unroll
                     for (int kk = 0; kk < kD / 32; ++kk)
                         mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
+                    tc_commit(B.k_empty + s);
                 }
-                tc_commit(B.done + b % kDoneBars);
+                tc_commit(B.s_ready + (b & 1));
             }
             tc_commit(B.drain);
             drain_wait(B.drain, 0, p.limit_ns);
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ PV issuer
+        // PV(j) once P(j) is written and V(j) has landed: [E | O] += P [ones ; V]
+        // (the 16 extra columns receive the row sums), the mean-restore MMA when
+        // due, then commits for the V stage and for s_ready (phase of block j+2).
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = make_idesc(128, 144, 0, 0);
+            constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
+            const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
+            const uint32_t tO = tmem + kTmemO;
+            // blocks 0 and 1 have no PV(b-2): their s_ready phases take a plain arrival
+            mbar_arrive(B.s_ready);
+            mbar_arrive(B.s_ready + 1);
+            for (int j = 0; j < nb; ++j) {
+                const int s = j % kVStages, pb = j & 1;
+                if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
+                if (!mbar_wait_spin(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
+                tc_fence_after();
+                const uint32_t vstage = sbase + kOffV + s * kVStageBytes;
+                const uint64_t dv = sdesc_k_sw128(pb == 0 ? vstage : vstage + kOnesBytes);
+                const uint32_t td = tmem + (pb == 0 ? kTmemE0 : kTmemO);
+                const uint32_t tp = tmem + kTmemP0 + 32 * pb;
+#pragma unroll
+                for (int kk = 0; kk < kBlk / 32; ++kk)
+                    mma_f8f6f4_ts(td, tp + 8 * kk, dv + 2 * kk, idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                if (flush_after(j)) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
+                }
+                tc_commit(B.v_empty + s);
+                tc_commit(B.s_ready + pb);
+            }
+            tc_commit(B.drain + 1);
+            drain_wait(B.drain + 1, 0, p.limit_ns);
         }
     } else {
         // ------------------------------------------------------------ softmax
@@ -315,7 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (b + 1 < nb) sk_next = skh[b + 1];
             // S(b) is ready, and with it PV(b-2): P buffer sb is free and the
             // row-sum slot of this parity holds block b-2's sums
-            bool wok = wait_done(B.done, b, abort_flag, p.limit_ns);
+            bool wok = wait_s_ready(B, b, abort_flag, p.limit_ns);
             wok = __all_sync(0xffffffffu, wok) && ok;
             uint32_t S[kCols];
             uint32_t rs_raw = 0;
@@ -397,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // MMA after it) finished
             if (rescale) {
                 const int jb = b - 1;
-                ok = __all_sync(0xffffffffu, wait_done(B.done, jb + 2, abort_flag, p.limit_ns));
+                ok = __all_sync(0xffffffffu, wait_s_ready(B, jb + 2, abort_flag, p.limit_ns));
                 if (ok) {
                     tc_fence_after();
 #pragma unroll 1
@@ -431,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ epilogue
         if (ok) {
             const int jb = nb - 1;
-            ok = __all_sync(0xffffffffu, wait_done(B.done, jb + 2, abort_flag, p.limit_ns));
+            ok = __all_sync(0xffffffffu, wait_s_ready(B, jb + 2, abort_flag, p.limit_ns));
         }
         // every softmax warp arrives here, whether it finished or gave up; the
         // epilogue (and its barriers) runs only if all of them finished
