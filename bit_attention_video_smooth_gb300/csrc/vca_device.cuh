@@ -389,7 +389,8 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // fp32 FMA t = fma(s, 8c, bias)
 // (packed two per instruction), rounding to an integer by adding 1.5 * 2^23,
 // then the clip: codes below 0 (and NaN) become 0 with one max, codes above 126
-// become 126 (kClip), and the bytes 1..7 are zeroed together: a byte b <= 126
+// become 126 (kClip), the codes are packed, and the bytes 1..7 are zeroed
+// together: a byte b <= 126
 // is >= 8 exactly when b + 120 has its top bit set, which PRMT replicates into
 // a byte mask.  Without kClip the caller guarantees codes <= 126: that holds
 // when fp32(s * c) <= fp32(m + 8) and |m| < 2^22, because t then exceeds
@@ -407,8 +408,13 @@ __device__ __forceinline__ uint32_t expcast4(uint64_t s01, uint64_t s23, uint64_
         x[e] = fmaxf(x[e], kMagic);
         if (kClip) x[e] = fminf(x[e], kMagic + 126.0f);
     }
-    const uint32_t w = prmt(prmt(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x0040),
-                            prmt(__float_as_uint(x[2]), __float_as_uint(x[3]), 0x0040), 0x5410);
+    // Gather the four low bytes: the pattern of x is 0x4B400000 + code, so its
+    // byte 1 is zero; one PRMT packs codes 0 and 1 over two zero bytes, and
+    // codes 2 and 3 are added in with integer multiply-adds, whose 0x4B40 high
+    // half vanishes (times 2^16 or 2^24, modulo 2^32).
+    uint32_t w = prmt(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x1140);
+    asm("mad.lo.u32 %0, %1, 65536, %0;" : "+r"(w) : "r"(__float_as_uint(x[2])));
+    asm("mad.lo.u32 %0, %1, 16777216, %0;" : "+r"(w) : "r"(__float_as_uint(x[3])));
     return w & prmt(w + 0x78787878u, 0u, 0xBA98);
 }
 
