@@ -118,18 +118,21 @@ template <bool kExpcast>
 __device__ __forceinline__ void write_codes(const uint32_t (&S)[kCols], float c, float m, uint32_t tp) {
     uint32_t w[kCols / 4];
     if constexpr (kExpcast) {
-        const float c8 = __fmul_rn(8.0f, c);
-        const float bias = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m));
-        const uint64_t c8x2 = pk2(__float_as_uint(c8), __float_as_uint(c8));
-        const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
+        // t / 256 = fma(S, 8c / 256, (55.65 - 8m) / 256), both scalings exact
+        const float c8s = __fmul_rn(c, 1.0f / 32.0f);
+        const float bs = __fmul_rn(__fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m)), 1.0f / 256.0f);
         if (__all_sync(0xffffffffu, fabsf(m) < kExpcastFastMax)) {
 #pragma unroll
-            for (int q = 0; q < kCols / 4; ++q)
-                w[q] = expcast4<false>(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), c8x2, c8x2, bx2, bx2);
+            for (int q = 0; q < kCols / 4; ++q) {
+                const uint32_t sv[4] = {S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]};
+                w[q] = expcast4<false>(sv, c8s, bs);
+            }
         } else {
 #pragma unroll
-            for (int q = 0; q < kCols / 4; ++q)
-                w[q] = expcast4<true>(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), c8x2, c8x2, bx2, bx2);
+            for (int q = 0; q < kCols / 4; ++q) {
+                const uint32_t sv[4] = {S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]};
+                w[q] = expcast4<true>(sv, c8s, bs);
+            }
         }
     } else {
         const float negm = -m;
@@ -525,20 +528,24 @@ __global__ void expcast_codes_kernel(const float *__restrict__ s_raw, const floa
                                      const float *__restrict__ m, int64_t n, uint8_t *__restrict__ out) {
     for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; 4 * g < n;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        uint32_t sv[4], c8[4], bias[4];
+        // the kernel's arithmetic, one scale per element: t / 256 from the
+        // exactly scaled factors
+        uint32_t w = 0;
         bool fast = true;
+        uint32_t sv[4];
+        float c8s[4], bs[4];
         for (int e = 0; e < 4; ++e) {
             const int64_t i = (4 * g + e < n) ? 4 * g + e : n - 1;
             sv[e] = __float_as_uint(s_raw[i]);
-            c8[e] = __float_as_uint(__fmul_rn(8.0f, c[i]));
-            bias[e] = __float_as_uint(__fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m[i])));
+            c8s[e] = __fmul_rn(c[i], 1.0f / 32.0f);
+            bs[e] = __fmul_rn(__fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m[i])), 1.0f / 256.0f);
             fast = fast && fabsf(m[i]) < kExpcastFastMax && __fmul_rn(s_raw[i], c[i]) <= __fadd_rn(m[i], 8.0f);
         }
-        const uint64_t s01 = pk2(sv[0], sv[1]), s23 = pk2(sv[2], sv[3]);
-        const uint32_t w = fast ? expcast4<false>(s01, s23, pk2(c8[0], c8[1]), pk2(c8[2], c8[3]),
-                                                  pk2(bias[0], bias[1]), pk2(bias[2], bias[3]))
-                                : expcast4<true>(s01, s23, pk2(c8[0], c8[1]), pk2(c8[2], c8[3]),
-                                                 pk2(bias[0], bias[1]), pk2(bias[2], bias[3]));
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t one[4] = {sv[e], sv[e], sv[e], sv[e]};
+            const uint32_t code = (fast ? expcast4<false>(one, c8s[e], bs[e]) : expcast4<true>(one, c8s[e], bs[e])) & 0xFFu;
+            w |= code << (8 * e);
+        }
         for (int e = 0; e < 4; ++e)
             if (4 * g + e < n) out[4 * g + e] = static_cast<uint8_t>((w >> (8 * e)) & 0xFFu);
     }

@@ -385,33 +385,35 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
-// Four ExpCast codes packed in one word (byte i = element i): per element one
-// fp32 FMA t = fma(s, 8c, bias)
-// (packed two per instruction), rounding to an integer by adding 1.5 * 2^23,
-// then the clip: codes below 0 (and NaN) become 0 with one max, codes above 126
-// become 126 (kClip), the codes are packed, and the bytes 1..7 are zeroed
-// together: a byte b <= 126
-// is >= 8 exactly when b + 120 has its top bit set, which PRMT replicates into
-// a byte mask.  Without kClip the caller guarantees codes <= 126: that holds
-// when fp32(s * c) <= fp32(m + 8) and |m| < 2^22, because t then exceeds
-// 55.65 by at most 8 * 8 + 16 ulp(m) <= 68.
+// Four ExpCast codes packed in one word (byte i = element i).  Per element one
+// saturating fp32 FMA forms u = t / 256 clamped to [0, 1]: with c8s = 8c / 256
+// and bs = (55.65 - 8m) / 256 (both exact, a power-of-two scaling), u is
+// fma(s, 8c, 55.65 - 8m) / 256 with the same single rounding, and negative t
+// and NaN give 0.  Adding 1.5 * 2^15 (ulp 2^-8, packed two per instruction)
+// rounds 256 u = t to an integer, nearest even, in the low mantissa bits: the
+// pattern is 0x47400000 + code.  kClip caps u at 126/256 (codes above 126
+// become 126).  The codes are packed with one PRMT for codes 0 and 1 (over the
+// pattern's zero byte 1) and integer multiply-adds for codes 2 and 3 (the
+// 0x4740 high half vanishes times 2^16 or 2^24, modulo 2^32), and the bytes
+// 1..7 are zeroed together: a byte b <= 126 is >= 8 exactly when b + 120 has
+// its top bit set, which PRMT replicates into a byte mask.  Without kClip the
+// caller guarantees codes <= 126: that holds when fp32(s * c) <= fp32(m + 8)
+// and |m| < 2^22, because t then exceeds 55.65 by at most 8 * 8 + 16 ulp(m)
+// <= 68.
 constexpr float kExpcastFastMax = 4194304.0f;   // 2^22
+constexpr float kMagicSat = 49152.0f;           // 1.5 * 2^15
 template <bool kClip>
-__device__ __forceinline__ uint32_t expcast4(uint64_t s01, uint64_t s23, uint64_t c8_01, uint64_t c8_23,
-                                             uint64_t b01, uint64_t b23) {
-    const uint64_t magic2 = pk2(__float_as_uint(kMagic), __float_as_uint(kMagic));
-    float x[4];
-    upk2(add2(fma2(s01, c8_01, b01), magic2), x[0], x[1]);
-    upk2(add2(fma2(s23, c8_23, b23), magic2), x[2], x[3]);
+__device__ __forceinline__ uint32_t expcast4(const uint32_t (&s)[4], float c8s, float bs) {
+    float u[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-        x[e] = fmaxf(x[e], kMagic);
-        if (kClip) x[e] = fminf(x[e], kMagic + 126.0f);
+        asm("fma.rn.sat.f32 %0, %1, %2, %3;" : "=f"(u[e]) : "f"(__uint_as_float(s[e])), "f"(c8s), "f"(bs));
+        if (kClip) u[e] = fminf(u[e], 126.0f / 256.0f);
     }
-    // Gather the four low bytes: the pattern of x is 0x4B400000 + code, so its
-    // byte 1 is zero; one PRMT packs codes 0 and 1 over two zero bytes, and
-    // codes 2 and 3 are added in with integer multiply-adds, whose 0x4B40 high
-    // half vanishes (times 2^16 or 2^24, modulo 2^32).
+    const uint64_t magic2 = pk2(__float_as_uint(kMagicSat), __float_as_uint(kMagicSat));
+    float x[4];
+    upk2(add2(pk2(__float_as_uint(u[0]), __float_as_uint(u[1])), magic2), x[0], x[1]);
+    upk2(add2(pk2(__float_as_uint(u[2]), __float_as_uint(u[3])), magic2), x[2], x[3]);
     uint32_t w = prmt(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x1140);
     asm("mad.lo.u32 %0, %1, 65536, %0;" : "+r"(w) : "r"(__float_as_uint(x[2])));
     asm("mad.lo.u32 %0, %1, 16777216, %0;" : "+r"(w) : "r"(__float_as_uint(x[3])));
