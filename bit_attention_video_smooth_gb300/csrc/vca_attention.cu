@@ -87,6 +87,7 @@ struct Params {
     int N;
     float scale_log2;
     uint64_t limit_ns;
+    uint32_t one;   // 1: an opaque multiplier for integer adds on the FMA pipe
 };
 
 // Two threads issue the MMAs: the QK thread (S(b) = Q K_b^T) and the PV thread
@@ -115,7 +116,7 @@ __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_
 // P codes of this thread's half row (64 keys) against the reference max m,
 // stored as 16 TMEM columns (four codes per column) of the P buffer at `tp`.
 template <bool kExpcast>
-__device__ __forceinline__ void write_codes(const uint32_t (&S)[kCols], float c, float m, uint32_t tp) {
+__device__ __forceinline__ void write_codes(const uint32_t (&S)[kCols], float c, float m, uint32_t tp, uint32_t one) {
     uint32_t w[kCols / 4];
     if constexpr (kExpcast) {
         // t / 256 = fma(S, 8c / 256, (55.65 - 8m) / 256), both scalings exact
@@ -125,13 +126,13 @@ __device__ __forceinline__ void write_codes(const uint32_t (&S)[kCols], float c,
 #pragma unroll
             for (int q = 0; q < kCols / 4; ++q) {
                 const uint32_t sv[4] = {S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]};
-                w[q] = expcast4<false>(sv, c8s, bs);
+                w[q] = expcast4<false>(sv, c8s, bs, one);
             }
         } else {
 #pragma unroll
             for (int q = 0; q < kCols / 4; ++q) {
                 const uint32_t sv[4] = {S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]};
-                w[q] = expcast4<true>(sv, c8s, bs);
+                w[q] = expcast4<true>(sv, c8s, bs, one);
             }
         }
     } else {
@@ -371,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 pm = row_part_max(S);
                 // codes against the current reference max, on the bet that this
                 // block does not move it (rewritten below when it does)
-                if (b > 0) write_codes<kExpcast>(S, c, m, tp);
+                if (b > 0) write_codes<kExpcast>(S, c, m, tp, p.one);
             }
             // Lazy reference-max update: only when the block's max exceeds m by
             // tau.  The block max moves m exactly when one part's max does
@@ -406,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S2 + 32 * i));
                     tmem_ld_wait();
-                    write_codes<kExpcast>(S2, c, m, tp);
+                    write_codes<kExpcast>(S2, c, m, tp, p.one);
                 }
                 rescale = __any_sync(0xffffffffu, alpha != 1.0f);
                 if (half == 0 && alpha != 1.0f) {
@@ -543,7 +544,7 @@ __global__ void expcast_codes_kernel(const float *__restrict__ s_raw, const floa
         }
         for (int e = 0; e < 4; ++e) {
             const uint32_t one[4] = {sv[e], sv[e], sv[e], sv[e]};
-            const uint32_t code = (fast ? expcast4<false>(one, c8s[e], bs[e]) : expcast4<true>(one, c8s[e], bs[e])) & 0xFFu;
+            const uint32_t code = (fast ? expcast4<false>(one, c8s[e], bs[e], 1u) : expcast4<true>(one, c8s[e], bs[e], 1u)) & 0xFFu;
             w |= code << (8 * e);
         }
         for (int e = 0; e < 4; ++e)
@@ -589,6 +590,7 @@ cudaError_t launch_attention(const AttentionArgs &a, cudaStream_t st) {
     p.N = a.N;
     p.scale_log2 = a.scale_log2;
     p.limit_ns = a.wait_limit_ns;
+    p.one = 1u;
     const dim3 grid(a.N / kBlk, a.BH);
     cudaError_t e;
     if (a.expcast) {

@@ -402,8 +402,11 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
 // <= 68.
 constexpr float kExpcastFastMax = 4194304.0f;   // 2^22
 constexpr float kMagicSat = 49152.0f;           // 1.5 * 2^15
+// `one` must hold 1: it turns the flush's integer add into a multiply-add,
+// which issues to the FMA pipe instead of the ALU pipe (the caller passes a
+// value the compiler cannot fold, e.g. a kernel parameter).
 template <bool kClip>
-__device__ __forceinline__ uint32_t expcast4(const uint32_t (&s)[4], float c8s, float bs) {
+__device__ __forceinline__ uint32_t expcast4(const uint32_t (&s)[4], float c8s, float bs, uint32_t one) {
     float u[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -417,7 +420,9 @@ __device__ __forceinline__ uint32_t expcast4(const uint32_t (&s)[4], float c8s, 
     uint32_t w = prmt(__float_as_uint(x[0]), __float_as_uint(x[1]), 0x1140);
     asm("mad.lo.u32 %0, %1, 65536, %0;" : "+r"(w) : "r"(__float_as_uint(x[2])));
     asm("mad.lo.u32 %0, %1, 16777216, %0;" : "+r"(w) : "r"(__float_as_uint(x[3])));
-    return w & prmt(w + 0x78787878u, 0u, 0xBA98);
+    uint32_t t;
+    asm("mad.lo.u32 %0, %1, %2, 2021161080;" : "=r"(t) : "r"(w), "r"(one));   // w + 0x78787878
+    return w & prmt(t, 0u, 0xBA98);
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
