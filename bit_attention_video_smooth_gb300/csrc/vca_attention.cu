@@ -9,32 +9,46 @@
 //   warp 0     TMA producer: K tiles into a 3-stage ring
 //   warp 10    TMA producer: V-residual tiles into a 3-stage ring
 //   warp 11    QK issuer (one thread): S[b&1] = Q8 K8_b^T (kind::f8f6f4,
-//              N = 128) once K(b) has landed and P(b-2) has been released
+//              N = 128) once K(b) has landed and S(b-2) has been read
 //   warp 1     TMEM owner and PV issuer (one thread):
 //                [E | O] += P_b [ones ; V8_b]       (kind::f8f6f4, N = 144): the
 //                         16 extra output columns are the block's row sums of the
 //                         decoded P, so the softmax threads never add them up
 //              and every 16 key blocks O += [rowsum hi|lo] [mean/s_v hi|lo]^T (bf16).
-//              Two issuing threads keep each one's serial work (barrier
-//              checks, MMA issue, commits) off the other's critical path.
-//   warps 2-9  softmax: two threads per query row -- the warps w and w+4 share
-//              a TMEM lane quarter and take the S columns 0-63 and 64-127; the
-//              pair exchanges its half-row maxima through shared memory at a
-//              64-thread named barrier.  Reference max with the lazy threshold
-//              (it moves only when a block's max exceeds it by 8), O rescaled in
-//              TMEM when it moves, P codes stored to TMEM (the A operand of PV);
-//              the row sum of block b-2 is read from its TMEM slot, brought to
-//              the current max and buffered for the mean restore; epilogue
+//   warps 2-9  softmax, one thread per query row and key block: the warps w and
+//              w+4 share a TMEM lane quarter (and a sub-partition) and take the
+//              even and the odd key blocks, whole rows of 128 scores each, so
+//              one of them computes while the other waits for its next block.
+//              The reference max is sequential over blocks: after its row max
+//              of block b, a thread takes the reference max after block b-1
+//              from its partner (shared memory + a named barrier), decides the
+//              max after block b (lazy threshold: it moves only when the block
+//              max exceeds it by 8) and hands it on before computing the codes,
+//              so every code is taken against its block's final reference max.
+//              O is rescaled in TMEM when the max moves; the row sum of block
+//              b-2 is read from its TMEM slot and kept, with the reference max
+//              it was taken against, for the mean restore; epilogue
 //              O = (O s_v + the last, partial group of mean terms) / l.
-// The issuing threads wait for P with non-suspending polls (they are on the
-// critical path); S[b&1] needs no signal of its own: every softmax warp reads
-// S(b-2) before it releases P(b-2), which the QK thread waits for.
+// Barriers between the softmax and the MMA threads, per parity of b:
+//   s_full  QK(b) committed: S(b) is in S[b&1]
+//   s_free  the four warps of the parity have read S(b): QK(b+2) may start
+//   p_full  the four warps have written P(b) (and cleared the row-sum slot)
+//   pv_done PV(b) (and the mean MMA after it) committed: P buffer b&1 and the
+//           row-sum slot b&1 are free, and the slot holds block b's sums.
+// A parity wait is only exact when the waiter is at most one phase behind the
+// barrier and has seen the phase before the one it waits for complete: each
+// thread waits on a barrier phase by phase (or, for the other parity's
+// pv_done, only after PV(b-2) and so PV(b-3) completed).  The MMA threads wait
+// with non-suspending polls (they are on the critical path).
 // TMEM columns: S0 [0,128), S1 [128,256), E0 [256,272), O [272,400), E1 [400,416),
 // P0 [416,448), P1 [448,480), Q [480,512).  Q and P, the A operands of the two
 // contractions, live in TMEM (four FP8 codes per column), so the tensor core
 // reads only K and V from shared memory.
-// Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
-// drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
+// Every wait on an mbarrier is bounded; a wait that runs out raises a CTA-wide
+// abort, the CTA drains its copies and MMAs, frees TMEM and reports
+// VCA_ERR_TIMEOUT.  Each named-barrier wait is matched by an arrival on every
+// path: a thread that gives up still hands on a reference max (NaN, which
+// makes its partner give up at its next block) before leaving the loop.
 #include "vca_attention_common.cuh"
 #include "vca_internal.h"
 
@@ -49,13 +63,13 @@ constexpr int kVStages = 3;               // V tiles in flight (released after t
 constexpr int kVWarp = 2 + kSoftmaxWarps;  // the V producer
 constexpr int kQKWarp = kVWarp + 1;        // the QK issuer (the PV issuer is warp 1)
 constexpr int kThreads = 32 * (kQKWarp + 1);
-constexpr int kRsCap = 32;                 // buffered row sums per row (<= 17 in use)
 constexpr uint32_t kTileBytes = kBlk * kD; // one 128 x 128 FP8 tile (16 KB)
 constexpr uint32_t kTmemCols = 512;
 // TMEM: S0 [0,128), S1 [128,256), row-sum slot E0 [256,272), O [272,400), E1 [400,416).
 // PV of an even block writes [E0 | O] (B = [ones ; V]), of an odd block [O | E1]
 // (B = [V ; ones]): the 16 extra output columns are the block's row sums.
 constexpr uint32_t kTmemE0 = 256, kTmemO = 272, kTmemE1 = 400, kTmemP0 = 416, kTmemQ = 480;
+constexpr uint32_t kBarHand0 = 2;          // + 2 * quarter + parity: the reference-max hand-over
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t kOffK = 0;
@@ -64,18 +78,19 @@ constexpr uint32_t kVStageBytes = kOnesBytes + kTileBytes + kOnesBytes;   // [on
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kOffMA = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
-constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128] buffered row sums
-constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128] residual scales
-constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
-constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
-constexpr uint32_t kOffBar = kOffL + kBlk * 4;
-constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 + 2 + 2;
+constexpr uint32_t kOffRS = kOffMB + kTileBytes;             // fp32 [kRsSlots][128] row sums (block j in slot j % 32)
+constexpr uint32_t kOffRSM = kOffRS + kRsSlots * kBlk * 4;   // fp32 [kRsSlots][128] the max each sum is taken against
+constexpr uint32_t kOffSV = kOffRSM + kRsSlots * kBlk * 4;   // fp32 [128] residual scales
+constexpr uint32_t kOffMX = kOffSV + kBlk * 4;               // fp32 [2][128] reference max handed over, per parity
+constexpr uint32_t kOffL = kOffMX + 2 * kBlk * 4;            // fp32 [128] l, [2][128] partial l, [2][128] their max
+constexpr uint32_t kOffBar = kOffL + 5 * kBlk * 4;
+constexpr int kNumBars = 1 + 2 * kKStages + 2 * kVStages + 2 * 4 + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Bars {
-    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *p_full, *s_ready, *drain;
+    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_empty, *s_full, *s_free, *p_full, *pv_done, *drain;
 };
 
 struct Params {
@@ -90,20 +105,16 @@ struct Params {
     uint32_t one;   // 1: an opaque multiplier for integer adds on the FMA pipe
 };
 
-// Two threads issue the MMAs: the QK thread (S(b) = Q K_b^T) and the PV thread
-// (O += P_j V_j and the mean-restore MMAs).  The softmax of block b waits on
-// s_ready[b & 1], whose phase completes on two tcgen05.commit arrivals: the QK
-// thread's after QK(b) (S(b) is in TMEM) and the PV thread's after PV(b-2)
-// (P buffer and row-sum slot b & 1 are free, and the slot holds block b-2's
-// sums).  Every waiter is at most one phase behind: the next phase of
-// s_ready[b & 1] needs PV(b), which needs the softmax's P(b).
-__device__ __forceinline__ bool wait_s_ready(const Bars &B, int b, int *abort, uint64_t limit_ns) {
-    return mbar_wait(B.s_ready + (b & 1), (b >> 1) & 1, abort, limit_ns);
+// A mean-restore MMA follows PV(b) for b = 19, 35, 51, ...: it adds the terms
+// of blocks b-19 .. b-4.  Their row sums are all visible to the thread that
+// stages them at block b (b is odd, so that thread takes the odd blocks): the
+// sum of an odd block j is written by the thread itself at block j+2 <= b-2,
+// the sum of an even block j <= b-5 by its partner at block j+2, before the
+// partner hands over the reference max at block j+4 <= b-1.
+constexpr int kMeanLag = 3;
+__host__ __device__ constexpr bool flush_after(int b) {
+    return b >= kMeanJ + kMeanLag && (b % kMeanJ) == kMeanLag;
 }
-
-// A mean-restore MMA follows PV(b) when the row sums of blocks b-17 .. b-2 are
-// all buffered (they are read two blocks late).
-__host__ __device__ constexpr bool flush_after(int b) { return b >= kMeanJ + 1 && (b % kMeanJ) == 1; }
 
 // exp2 then E4M3 for four raw scores: p = 2^(fma(S, c, -m)).
 __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_t cx2, uint64_t negmx2) {
@@ -113,25 +124,28 @@ __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_
     return e4m3x2(ex2_approx(a[0]), ex2_approx(a[1])) | (e4m3x2(ex2_approx(a[2]), ex2_approx(a[3])) << 16);
 }
 
-// P codes of this thread's half row (64 keys) against the reference max m,
-// stored as 16 TMEM columns (four codes per column) of the P buffer at `tp`.
-template <bool kExpcast>
-__device__ __forceinline__ void write_codes(const uint32_t (&S)[kCols], float c, float m, uint32_t tp, uint32_t one) {
-    uint32_t w[kCols / 4];
+// P codes of 32 keys (X[kOff .. kOff+31]) against the reference max m of the
+// block, stored as 8 TMEM columns (four codes per column) at tp.  `fast`
+// (warp-uniform) says |m| < 2^22, so that the ExpCast codes need no clip: m is
+// the block's final reference max, so every score satisfies s c <= m + 8.
+template <bool kExpcast, int kOff>
+__device__ __forceinline__ void write_codes32(const uint32_t (&X)[kCols], float c, float m, bool fast,
+                                              uint32_t tp, uint32_t one) {
+    uint32_t w[8];
     if constexpr (kExpcast) {
         // t / 256 = fma(S, 8c / 256, (55.65 - 8m) / 256), both scalings exact
         const float c8s = __fmul_rn(c, 1.0f / 32.0f);
         const float bs = __fmul_rn(__fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m)), 1.0f / 256.0f);
-        if (__all_sync(0xffffffffu, fabsf(m) < kExpcastFastMax)) {
+        if (fast) {
 #pragma unroll
-            for (int q = 0; q < kCols / 4; ++q) {
-                const uint32_t sv[4] = {S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]};
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t sv[4] = {X[kOff + 4 * q], X[kOff + 4 * q + 1], X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]};
                 w[q] = expcast4<false>(sv, c8s, bs, one);
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < kCols / 4; ++q) {
-                const uint32_t sv[4] = {S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]};
+            for (int q = 0; q < 8; ++q) {
+                const uint32_t sv[4] = {X[kOff + 4 * q], X[kOff + 4 * q + 1], X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]};
                 w[q] = expcast4<true>(sv, c8s, bs, one);
             }
         }
@@ -140,16 +154,36 @@ __device__ __forceinline__ void write_codes(const uint32_t (&S)[kCols], float c,
         const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
         const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
 #pragma unroll
-        for (int q = 0; q < kCols / 4; ++q)
-            w[q] = expconv4(pk2(S[4 * q], S[4 * q + 1]), pk2(S[4 * q + 2], S[4 * q + 3]), cx2, nx2);
+        for (int q = 0; q < 8; ++q)
+            w[q] = expconv4(pk2(X[kOff + 4 * q], X[kOff + 4 * q + 1]), pk2(X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]),
+                            cx2, nx2);
     }
-    if constexpr (kCols == 64) {
-        VCA_TMEM_ST16(tp, w);
-    } else {
-        asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tp), "r"(w[0]),
-                     "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                     : "memory");
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tp), "r"(w[0]),
+                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+// Operands of the mean-restore MMA for blocks b0 .. b0+15 (row / channel
+// `row`): A row = the row sums from their ring slots, each brought from the
+// reference max it was taken against to m; B row = mean / s_v.
+__device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
+                                            const uint16_t *vmh, const float *sSV, unsigned char *sMA,
+                                            unsigned char *sMB) {
+    float hi[kMeanJ], lo[kMeanJ];
+#pragma unroll
+    for (int i = 0; i < kMeanJ; ++i) {
+        const int slot = ((b0 + i) & (kRsSlots - 1)) * kBlk + row;
+        float rs = sRS[slot];
+        const float mt = sRSM[slot];
+        if (mt != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mt, m)));
+        split_bf16(rs, hi[i], lo[i]);
     }
+    store_mean_row(sMA, row, hi, lo, true);
+    const float inv_sv = 1.0f / sSV[row];
+#pragma unroll
+    for (int i = 0; i < kMeanJ; ++i)
+        split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
+    store_mean_row(sMB, row, hi, lo, false);
 }
 
 template <bool kExpcast>
@@ -166,15 +200,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     B.k_empty = B.k_full + kKStages;
     B.v_full = B.k_empty + kKStages;
     B.v_empty = B.v_full + kVStages;
-    B.p_full = B.v_empty + kVStages;
-    B.s_ready = B.p_full + 2;
-    B.drain = B.s_ready + 2;   // [0]: QK thread, [1]: PV thread
+    B.s_full = B.v_empty + kVStages;
+    B.s_free = B.s_full + 2;
+    B.p_full = B.s_free + 2;
+    B.pv_done = B.p_full + 2;
+    B.drain = B.pv_done + 2;   // [0]: QK thread, [1]: PV thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_flag = reinterpret_cast<int *>(smem + kOffMisc + 4);
     float *sRS = reinterpret_cast<float *>(smem + kOffRS);
+    float *sRSM = reinterpret_cast<float *>(smem + kOffRSM);
     float *sSV = reinterpret_cast<float *>(smem + kOffSV);
-    float *sPM = reinterpret_cast<float *>(smem + kOffPM);
+    float *sMX = reinterpret_cast<float *>(smem + kOffMX);
     float *sL = reinterpret_cast<float *>(smem + kOffL);
+    float *sLp = sL + kBlk;        // [2][128] partial row sums, per parity
+    float *sMp = sL + 3 * kBlk;    // [2][128] the reference max they are taken against
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qtile = blockIdx.x, bh = blockIdx.y;
@@ -191,8 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(B.v_empty + s, 1);
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(B.p_full + i, kSoftmaxWarps);
-            mbar_init(B.s_ready + i, 2);   // QK(b) and PV(b-2)
+            mbar_init(B.s_full + i, 1);
+            mbar_init(B.s_free + i, kSoftmaxWarps / 2);
+            mbar_init(B.p_full + i, kSoftmaxWarps / 2);
+            mbar_init(B.pv_done + i, 1);
             mbar_init(B.drain + i, 1);
         }
         *abort_flag = 0;
@@ -248,29 +289,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == kQKWarp) {
         // ------------------------------------------------------------ QK issuer
-        // QK(b) into S[b & 1] once K(b) has landed and the softmax has released
-        // P(b-2) (it reads S(b-2) out of S[b & 1] before that); then commits
-        // for the K stage and for s_ready.  Steps nb and nb+1 issue no MMA but
-        // still wait for P(b-2) and commit, so that the last two phases of
-        // s_ready (the epilogue waits for them) complete, each only after the
-        // phase before it on the same barrier.
+        // QK(b) into S[b & 1] once K(b) has landed and the softmax has read
+        // S(b-2) out of that buffer; commits for the K stage and for s_full.
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc(128, 128, 0, 0);
             const uint32_t sbase = smem_u32(smem);
             bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
-            for (int b = 0; ok && b < nb + 2; ++b) {
-                if (b >= 2 && !mbar_wait_spin(B.p_full + (b & 1), ((b - 2) >> 1) & 1, abort_flag, p.limit_ns)) break;
-                if (b < nb) {
-                    const int s = b % kKStages, sb = b & 1;
-                    if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) break;
-                    tc_fence_after();
-                    const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
+            for (int b = 0; ok && b < nb; ++b) {
+                const int s = b % kKStages, sb = b & 1;
+                if (b >= 2 && !mbar_wait_spin(B.s_free + sb, ((b - 2) >> 1) & 1, abort_flag, p.limit_ns)) break;
+                if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) break;
+                tc_fence_after();
+                const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kD / 32; ++kk)
-                        mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
-                    tc_commit(B.k_empty + s);
-                }
-                tc_commit(B.s_ready + (b & 1));
+                for (int kk = 0; kk < kD / 32; ++kk)
+                    mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
+                tc_commit(B.k_empty + s);
+                tc_commit(B.s_full + sb);
             }
             tc_commit(B.drain);
             drain_wait(B.drain, 0, p.limit_ns);
@@ -279,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ PV issuer
         // PV(j) once P(j) is written and V(j) has landed: [E | O] += P [ones ; V]
         // (the 16 extra columns receive the row sums), the mean-restore MMA when
-        // due, then commits for the V stage and for s_ready (phase of block j+2).
+        // due, then commits for the V stage and for pv_done.
         if (lane == 0) {
             constexpr uint32_t idesc_pv = make_idesc(128, 144, 0, 0);
             constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
@@ -287,9 +322,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
             const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
             const uint32_t tO = tmem + kTmemO;
-            // blocks 0 and 1 have no PV(b-2): their s_ready phases take a plain arrival
-            mbar_arrive(B.s_ready);
-            mbar_arrive(B.s_ready + 1);
             for (int j = 0; j < nb; ++j) {
                 const int s = j % kVStages, pb = j & 1;
                 if (!mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
@@ -307,7 +339,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
                 }
                 tc_commit(B.v_empty + s);
-                tc_commit(B.s_ready + pb);
+                tc_commit(B.pv_done + pb);
             }
             tc_commit(B.drain + 1);
             drain_wait(B.drain + 1, 0, p.limit_ns);
@@ -315,195 +347,199 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ softmax
         const int quarter = warp & 3;                              // TMEM lane quarter
-        const int half = (warp - 2) >> 2;                          // column part: S columns kCols*half ..
+        const int par = (warp - 2) >> 2;                           // this warp's key blocks: par, par + 2, ...
         const int row = quarter * 32 + lane;                       // query row in the tile == TMEM lane
-        const uint32_t pair_bar = kBarPair0 + quarter;
-        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t col0 = static_cast<uint32_t>(kCols) * half;
-        const uint32_t tO = tmem + lane_base + kTmemO + col0;
+        const uint32_t bar_out = kBarHand0 + 2 * quarter + par;    // hands the reference max on
+        const uint32_t bar_in = kBarHand0 + 2 * quarter + (par ^ 1);
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
         const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
         unsigned char *sMA = smem + kOffMA;
         unsigned char *sMB = smem + kOffMB;
         const float kNegInf = __int_as_float(0xff800000);
-        float m = kNegInf, mh1 = kNegInf, mh2 = kNegInf;   // running max; the max of blocks b-1, b-2
-        float l = 0.0f;                                    // kept by the half-0 thread of the row
-        int rs_cnt = 0;
+        float m = kNegInf;   // reference max after this thread's latest block
+        float l = 0.0f;      // row sum of this thread's blocks, taken against m
         bool ok = true;
-        float sk_next = skh[0];
-        if (half == 0) {
+        if (par == 0) {
             // Q tile into TMEM (the A operand of QK): this row's 128 codes, 32 columns
             load_q_row(p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD,
-                       tmem + lane_base + kTmemQ);
+                       tl + kTmemQ);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(B.q_full);
         }
-        for (int b = 0; b < nb; ++b) {
+        float sk_next = par < nb ? skh[par] : 0.0f;
+        for (int b = par; b < nb; b += 2) {
             const int sb = b & 1;
             const float sk_b = sk_next;
-            if (b + 1 < nb) sk_next = skh[b + 1];
-            // S(b) is ready, and with it PV(b-2): P buffer sb is free and the
-            // row-sum slot of this parity holds block b-2's sums
-            bool wok = wait_s_ready(B, b, abort_flag, p.limit_ns);
-            wok = __all_sync(0xffffffffu, wok) && ok;
-            uint32_t S[kCols];
-            uint32_t rs_raw = 0;
-            float pm = kNegInf;
+            if (b + 2 < nb) sk_next = skh[b + 2];
             const float c = __fmul_rn(__fmul_rn(sqv, sk_b), p.scale_log2);
-            const uint32_t tp = tmem + lane_base + kTmemP0 + 32 * sb + (kCols / 4) * half;
+            const uint32_t tS = tl + sb * 128;
+            // the row max of S(b); X keeps columns 64..127
+            uint32_t X[kCols];
+            float pm = kNegInf;
+            const bool wok = ok && __all_sync(0xffffffffu, mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns));
             if (wok) {
                 tc_fence_after();
-                const uint32_t tS = tmem + lane_base + sb * 128 + col0;
-#pragma unroll
-                for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S + 32 * i));
-                // half 0 owns the row-sum slot of this parity: read block b-2's
-                // sum, then clear the slot for PV(b) (PV(0) initialises E0 itself)
-                const uint32_t te = tmem + lane_base + (sb == 0 ? kTmemE0 : kTmemE1);
-                if (half == 0 && b >= 2)
-                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
+                VCA_TMEM_LD32(tS, X);
+                VCA_TMEM_LD32(tS + 32, (X + 32));
                 tmem_ld_wait();
-                if (half == 0 && b >= 1)   // completes before P(b) is released
+                pm = row_part_max(X);
+                VCA_TMEM_LD32(tS + 64, X);
+                VCA_TMEM_LD32(tS + 96, (X + 32));
+                tmem_ld_wait();
+                pm = fmaxf(pm, row_part_max(X));
+            }
+            // reference max after block b-1 (from the partner), after block b
+            // (handed on); NaN marks a partner that gave up
+            float m_in = kNegInf;
+            if (b >= 1) {
+                bar_sync(bar_in, 64);
+                m_in = sMX[(sb ^ 1) * kBlk + row];
+            }
+            const bool valid = wok && !(m_in != m_in);
+            const float bm = __fmul_rn(pm, c);
+            const bool moved = valid && bm > __fadd_rn(m_in, kLazyTau);
+            const float m_new = moved ? bm : m_in;
+            if (b + 1 < nb) {
+                sMX[sb * kBlk + row] = valid ? m_new : __int_as_float(0x7fc00000);
+                bar_arrive_release(bar_out, 64);
+            }
+            if (!__all_sync(0xffffffffu, valid)) {
+                ok = false;
+                break;
+            }
+            // P buffer b&1 and row-sum slot b&1 are free once PV(b-2) completed
+            if (b >= 2) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + sb, ((b - 2) >> 1) & 1, abort_flag, p.limit_ns));
+            if (ok) {
+                tc_fence_after();
+                const uint32_t tp = tl + kTmemP0 + 32 * sb;
+                const bool fast = __all_sync(0xffffffffu, fabsf(m_new) < kExpcastFastMax);
+                // codes of columns 64..127 from X, reloading columns 0..63 behind them
+                write_codes32<kExpcast, 0>(X, c, m_new, fast, tp + 16, p.one);
+                VCA_TMEM_LD32(tS, X);
+                write_codes32<kExpcast, 32>(X, c, m_new, fast, tp + 24, p.one);
+                VCA_TMEM_LD32(tS + 32, (X + 32));
+                // block b-2's row sum from the slot of this parity
+                const uint32_t te = tl + (sb == 0 ? kTmemE0 : kTmemE1);
+                uint32_t rs_raw = 0;
+                if (b >= 2) asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
+                tmem_ld_wait();
+                // S(b) is read: QK(b+2) may overwrite the buffer
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(B.s_free + sb);
+                // clear the slot for PV(b) (PV(0) initialises E0); completes before P(b) is released
+                if (b >= 1)
                     asm volatile(
                         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
                         ::"r"(te), "r"(0u) : "memory");
-                pm = row_part_max(S);
-                // codes against the current reference max, on the bet that this
-                // block does not move it (rewritten below when it does)
-                if (b > 0) write_codes<kExpcast>(S, c, m, tp, p.one);
-            }
-            // Lazy reference-max update: only when the block's max exceeds m by
-            // tau.  The block max moves m exactly when one part's max does
-            // (scaling by c >= 0 is monotone), so the common case takes one pair
-            // barrier: every thread of the row finished its wait and no part
-            // moves m.  Otherwise the parts exchange their maxima.
-            const float lim = __fadd_rn(m, kLazyTau);
-            const bool quiet = bar_and(wok && !(__fmul_rn(pm, c) > lim), pair_bar, 32 * kParts);
-            float alpha = 1.0f;
-            bool rescale = false;
-            if (!quiet) {
-                sPM[(sb * kParts + half) * kBlk + row] = pm;
-                ok = bar_and(wok, pair_bar, 32 * kParts);
-                if (!ok) break;
-                float smax = pm;
-#pragma unroll
-                for (int q = 1; q < kParts; ++q)
-                    smax = fmaxf(smax, sPM[(sb * kParts + ((half + q) % kParts)) * kBlk + row]);
-                const float bm = __fmul_rn(smax, c);
-                const bool moved = bm > lim;
-                if (moved) {
-                    if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
-                    m = bm;
+                write_codes32<kExpcast, 0>(X, c, m_new, fast, tp, p.one);
+                write_codes32<kExpcast, 32>(X, c, m_new, fast, tp + 8, p.one);
+                if (b >= 2) {
+                    // block b-2's sum, taken against m (this thread's max after b-2)
+                    const float rs = __uint_as_float(rs_raw);
+                    const int slot = ((b - 2) & (kRsSlots - 1)) * kBlk + row;
+                    sRS[slot] = rs;
+                    sRSM[slot] = m;
+                    l = __fadd_rn(l, rs);
+                    if (m != m_new) l = __fmul_rn(l, ex2_approx(__fsub_rn(m, m_new)));
                 }
-                if (__any_sync(0xffffffffu, moved)) {
-                    // S(b) is still in TMEM (S[b&1] is rewritten only after P(b) is
-                    // released): reload it rather than keep 64 registers live
-                    // through the code computation for this rare path
-                    tmem_st_wait();   // the optimistic codes land before they are replaced
-                    uint32_t S2[kCols];
-                    const uint32_t tS = tmem + lane_base + sb * 128 + col0;
-#pragma unroll
-                    for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S2 + 32 * i));
-                    tmem_ld_wait();
-                    write_codes<kExpcast>(S2, c, m, tp, p.one);
-                }
-                rescale = __any_sync(0xffffffffu, alpha != 1.0f);
-                if (half == 0 && alpha != 1.0f) {
-                    l = __fmul_rn(l, alpha);
+                // the reference max moved at block b: O (after PV(b-1)) from m_in to m_new
+                const float alpha = (moved && b > 0) ? ex2_approx(__fsub_rn(m_in, m_new)) : 1.0f;
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(B.pv_done + (sb ^ 1), ((b - 1) >> 1) & 1, abort_flag, p.limit_ns));
+                    if (ok) {
+                        tc_fence_after();
 #pragma unroll 1
-                    for (int i = 0; i < rs_cnt; ++i) sRS[i * kBlk + row] = __fmul_rn(sRS[i * kBlk + row], alpha);
-                }
-            }
-            if (half == 0 && b >= 2) {
-                // row sum of block b-2, taken against that block's max: bring it to m
-                float rs = __uint_as_float(rs_raw);
-                if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
-                l = __fadd_rn(l, rs);
-                sRS[rs_cnt * kBlk + row] = rs;
-            }
-            if (b >= 2) ++rs_cnt;
-
-            // rescale this half of the O accumulator after PV(b-1) (and any mean
-            // MMA after it) finished
-            if (rescale) {
-                const int jb = b - 1;
-                ok = __all_sync(0xffffffffu, wait_s_ready(B, jb + 2, abort_flag, p.limit_ns));
-                if (ok) {
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int i = 0; i < kCols / 32; ++i) {
-                        uint32_t o[32];
-                        VCA_TMEM_LD32(tO + 32 * i, o);
-                        tmem_ld_wait();
+                        for (int i = 0; i < kD / 32; ++i) {
+                            uint32_t o[32];
+                            VCA_TMEM_LD32(tl + kTmemO + 32 * i, o);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
-                        VCA_TMEM_ST32(tO + 32 * i, o);
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
+                            VCA_TMEM_ST32(tl + kTmemO + 32 * i, o);
+                        }
                     }
+                }
+                if (ok && flush_after(b)) {
+                    // mean-restore operands of blocks b-19 .. b-4 (the MMA follows PV(b))
+                    stage_means(row, sRS, sRSM, m_new, b - kMeanJ - kMeanLag, vmh, sSV, sMA, sMB);
+                    fence_proxy_async_smem();   // read by the tensor core
+                }
+                if (ok) {
                     tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B.p_full + sb);
                 }
             }
-
-            if (ok && flush_after(b)) {
-                // row sums of blocks b0 .. b0+15 (all at the current max)
-                stage_mean_operands(half, row, sRS, vmh, b - kMeanJ - 1, sSV, sMA, sMB);
-                rs_cnt = 0;
-                fence_proxy_async_smem();   // the mean operands are read by the tensor core
-            }
-            if (ok) {
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B.p_full + sb);
-            }
-            mh2 = mh1;
-            mh1 = m;
+            m = m_new;
         }
         // ------------------------------------------------------------ epilogue
-        if (ok) {
-            const int jb = nb - 1;
-            ok = __all_sync(0xffffffffu, wait_s_ready(B, jb + 2, abort_flag, p.limit_ns));
+        // this thread's last block lb: once PV(lb) has completed, its row sum
+        // is in the slot of this parity.  The wait is on this parity's barrier,
+        // whose previous phase (PV(lb-2)) this thread has seen complete: a
+        // parity wait for a phase two ahead of the barrier would return at once.
+        const int lb = (((nb - 1) & 1) == par) ? nb - 1 : nb - 2;
+        if (ok && lb >= 0)
+            ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + par, (lb >> 1) & 1, abort_flag, p.limit_ns));
+        if (ok && lb >= 0) {
+            tc_fence_after();
+            uint32_t r = 0;
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
+                         : "=r"(r)
+                         : "r"(tl + (par == 0 ? kTmemE0 : kTmemE1)));
+            tmem_ld_wait();
+            const float rs = __uint_as_float(r);
+            const int slot = (lb & (kRsSlots - 1)) * kBlk + row;
+            sRS[slot] = rs;
+            sRSM[slot] = m;
+            l = __fadd_rn(l, rs);
         }
+        sLp[par * kBlk + row] = l;
+        sMp[par * kBlk + row] = lb >= 0 ? m : kNegInf;
         // every softmax warp arrives here, whether it finished or gave up; the
         // epilogue (and its barriers) runs only if all of them finished
+        // PV(nb-1), and with it every MMA, has completed once the threads of its
+        // parity have passed their wait above
         ok = bar_and(ok, kBarSoftmax, 32 * kSoftmaxWarps);
         if (ok) {
             tc_fence_after();
-            if (half == 0) {
-                // the last two blocks' row sums
-                uint32_t r2 = 0, r1 = 0;
-                const uint32_t te0 = tmem + lane_base + kTmemE0, te1 = tmem + lane_base + kTmemE1;
-                const uint32_t te_last = ((nb - 1) & 1) ? te1 : te0, te_prev = ((nb - 1) & 1) ? te0 : te1;
-                if (nb >= 2)
-                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r2) : "r"(te_prev));
-                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r1) : "r"(te_last));
-                tmem_ld_wait();
-                int cnt = rs_cnt;
-                if (nb >= 2) {
-                    float rs = __uint_as_float(r2);
-                    if (mh2 != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mh2, m)));
-                    l = __fadd_rn(l, rs);
-                    sRS[cnt * kBlk + row] = rs;
-                    ++cnt;
+            // the blocks after the last mean MMA's range
+            const int bf = nb - 1 >= kMeanJ + kMeanLag ? kMeanLag + kMeanJ * ((nb - 1 - kMeanLag) / kMeanJ) : -1;
+            const int tail0 = bf >= 0 ? bf - kMeanLag : 0;
+            const int rs_cnt = nb - tail0;
+            const float mf = sMp[((nb - 1) & 1) * kBlk + row];   // the final reference max
+            if (par == 0) {
+                float lt = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float mq = sMp[q * kBlk + row];
+                    if (mq != kNegInf)
+                        lt = __fadd_rn(lt, mq == mf ? sLp[q * kBlk + row]
+                                                    : __fmul_rn(sLp[q * kBlk + row], ex2_approx(__fsub_rn(mq, mf))));
                 }
-                const float rs = __uint_as_float(r1);   // taken against m itself
-                l = __fadd_rn(l, rs);
-                sRS[cnt * kBlk + row] = rs;
-                sL[row] = l;
+                sL[row] = lt;
+                for (int t = 0; t < rs_cnt; ++t) {
+                    const int slot = ((tail0 + t) & (kRsSlots - 1)) * kBlk + row;
+                    if (sRSM[slot] != mf) sRS[slot] = __fmul_rn(sRS[slot], ex2_approx(__fsub_rn(sRSM[slot], mf)));
+                }
             }
-            rs_cnt += (nb >= 2) ? 2 : 1;
-            // the blocks since the last mean MMA: stage their means (fp32) in the
-            // mean-B buffer, whose last reader (the final mean MMA) has finished
-            const int tail0 = nb - rs_cnt;
+            // the tail blocks' means (fp32) in the mean-B buffer, whose last
+            // reader (the final mean MMA) has finished
             float *sMu = reinterpret_cast<float *>(sMB);
-            bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             for (int i = threadIdx.x - 64; i < rs_cnt * kD; i += 32 * kSoftmaxWarps)
                 sMu[i] = bf16_bits_to_f32(vmh[(tail0 + i / kD) * kD + (i % kD)]);
             bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             const float inv_l = 1.0f / sL[row];
+            const int col0 = kCols * par;
             uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD + col0;
-            store_output(tO, sSV, sRS, sMu, rs_cnt, row, static_cast<int>(col0), inv_l, orow);
+            store_output(tl + kTmemO + col0, sSV, sRS, sMu, rs_cnt, tail0, row, col0, inv_l, orow);
         }
     }
 
@@ -517,9 +553,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         atomicExch(p.dev_status, kErrTimeout);
 }
 
-// --------------------------------------------------------------------------
-// Host side: tensor maps and launch
-// --------------------------------------------------------------------------
 // ExpCast map alone, for bit-exact tests of the device function.
 // Four elements per thread through the same packed path the attention kernel
 // uses.  The unclipped variant is taken where the attention kernel would take

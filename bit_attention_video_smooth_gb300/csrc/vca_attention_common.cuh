@@ -65,6 +65,33 @@ __device__ __forceinline__ bool bar_and(bool v, uint32_t id, uint32_t count) {
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
+// Signal a named barrier without waiting (the producer side of bar.sync),
+// after a CTA-scope fence: the shared-memory writes before it are visible to
+// the threads that wait on the barrier.
+__device__ __forceinline__ void bar_arrive_release(uint32_t id, uint32_t count) {
+    asm volatile("fence.acq_rel.cta;\n\tbar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// One row of a mean-restore operand from kMeanJ values split as hi + lo bf16,
+// into the 128-byte-swizzled K-major tile `dst`:
+//   A (query row): [hi | lo | hi | lo]   (chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo)
+//   B (channel):   [hi | hi | lo | lo]   (chunks 0-3 hi; 4-7 lo)
+__device__ __forceinline__ void store_mean_row(unsigned char *dst, int row, const float (&hi)[kMeanJ],
+                                               const float (&lo)[kMeanJ], bool a_operand) {
+    uint4 hv[2], lv[2];
+#pragma unroll
+    for (int g = 0; g < 2; ++g) {
+        hv[g] = make_uint4(pack_bf16x2(hi[8 * g + 0], hi[8 * g + 1]), pack_bf16x2(hi[8 * g + 2], hi[8 * g + 3]),
+                           pack_bf16x2(hi[8 * g + 4], hi[8 * g + 5]), pack_bf16x2(hi[8 * g + 6], hi[8 * g + 7]));
+        lv[g] = make_uint4(pack_bf16x2(lo[8 * g + 0], lo[8 * g + 1]), pack_bf16x2(lo[8 * g + 2], lo[8 * g + 3]),
+                           pack_bf16x2(lo[8 * g + 4], lo[8 * g + 5]), pack_bf16x2(lo[8 * g + 6], lo[8 * g + 7]));
+    }
+#pragma unroll
+    for (int ck = 0; ck < 8; ++ck) {
+        const bool use_lo = a_operand ? (((ck >> 1) & 1) != 0) : (ck >= 4);
+        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ck)) = use_lo ? lv[ck & 1] : hv[ck & 1];
+    }
+}
 
 // Operands of one mean-restore MMA for key blocks b0 .. b0+kMeanJ-1, written
 // by the two threads of query row / channel `row`:
@@ -83,29 +110,17 @@ __device__ __forceinline__ void stage_mean_operands(int half, int row, const flo
         for (int i = 0; i < kMeanJ; ++i)
             split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
     }
-    unsigned char *dst = half == 0 ? sMA : sMB;
-    uint4 hv[2], lv[2];
-#pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        hv[g] = make_uint4(pack_bf16x2(hi[8 * g + 0], hi[8 * g + 1]), pack_bf16x2(hi[8 * g + 2], hi[8 * g + 3]),
-                           pack_bf16x2(hi[8 * g + 4], hi[8 * g + 5]), pack_bf16x2(hi[8 * g + 6], hi[8 * g + 7]));
-        lv[g] = make_uint4(pack_bf16x2(lo[8 * g + 0], lo[8 * g + 1]), pack_bf16x2(lo[8 * g + 2], lo[8 * g + 3]),
-                           pack_bf16x2(lo[8 * g + 4], lo[8 * g + 5]), pack_bf16x2(lo[8 * g + 6], lo[8 * g + 7]));
-    }
-#pragma unroll
-    for (int ck = 0; ck < 8; ++ck) {
-        // A: chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo.   B: chunks 0-3 hi; 4-7 lo.
-        const bool use_lo = (half == 0) ? (((ck >> 1) & 1) != 0) : (ck >= 4);
-        *reinterpret_cast<uint4 *>(dst + sw128_offset(row, ck)) = use_lo ? lv[ck & 1] : hv[ck & 1];
-    }
+    store_mean_row(half == 0 ? sMA : sMB, row, hi, lo, half == 0);
 }
 
 // O row part = (O_acc s_v + sum_t rs_t mu_t) / l for this thread's kCols
 // channels starting at col0: tO is the TMEM address of those accumulator
 // columns in this thread's lane, sMu the fp32 means [t][128] of the rs_cnt
-// blocks since the last mean MMA, orow the output row at col0.
+// blocks since the last mean MMA, whose row sums are in sRS slots
+// (slot0 + t) % kRsSlots; orow the output row at col0.
+constexpr int kRsSlots = 32;   // row-sum slots per query row (a ring)
 __device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, const float *sRS, const float *sMu,
-                                             int rs_cnt, int row, int col0, float inv_l, uint16_t *orow) {
+                                             int rs_cnt, int slot0, int row, int col0, float inv_l, uint16_t *orow) {
 #pragma unroll 1
     for (int i = 0; i < kCols / 32; ++i) {
         uint32_t o[32];
@@ -116,7 +131,7 @@ __device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, cons
         for (int e = 0; e < 32; ++e) acc[e] = __fmul_rn(__uint_as_float(o[e]), sSV[col0 + 32 * i + e]);
 #pragma unroll 1
         for (int t = 0; t < rs_cnt; ++t) {
-            const float r = sRS[t * kBlk + row];
+            const float r = sRS[((slot0 + t) & (kRsSlots - 1)) * kBlk + row];
             const float *mu = sMu + t * kD + col0 + 32 * i;
 #pragma unroll
             for (int e = 0; e < 32; ++e) acc[e] = __fmaf_rn(r, mu[e], acc[e]);

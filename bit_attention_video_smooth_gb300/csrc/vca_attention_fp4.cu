@@ -511,7 +511,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             const float inv_l = 1.0f / sL[row];
             uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD + col0;
-            store_output(tO, sSV, sRS, sMu, rs_cnt, row, static_cast<int>(col0), inv_l, orow);
+            store_output(tO, sSV, sRS, sMu, rs_cnt, 0, row, static_cast<int>(col0), inv_l, orow);
         }
     }
 

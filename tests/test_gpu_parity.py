@@ -187,7 +187,8 @@ def _prepped_both(V, orc, BH, N, seed, vmode=0):
 
 
 @pytest.mark.parametrize("expcast", [1, 0])
-@pytest.mark.parametrize("BH,N,seed", [(2, 1024, 0), (1, 128, 1), (3, 384, 2), (1, 2304, 3), (2, 4096, 4)])
+@pytest.mark.parametrize("BH,N,seed", [(2, 1024, 0), (1, 128, 1), (1, 256, 5), (3, 384, 2), (2, 640, 6), (1, 2304, 3),
+                                        (2, 4096, 4)])
 def test_attention_parity_on_oracle_operands(V, orc, expcast, BH, N, seed):
     ref, p = _prepped_both(V, orc, BH, N, seed)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
