@@ -125,13 +125,13 @@ __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_
 }
 
 // P codes of 32 keys (X[kOff .. kOff+31]) against the reference max m of the
-// block, stored as 8 TMEM columns (four codes per column) at tp.  `fast`
-// (warp-uniform) says |m| < 2^22, so that the ExpCast codes need no clip: m is
-// the block's final reference max, so every score satisfies s c <= m + 8.
-template <bool kExpcast, int kOff>
-__device__ __forceinline__ void write_codes32(const uint32_t (&X)[kCols], float c, float m, bool fast,
-                                              uint32_t tp, uint32_t one) {
-    uint32_t w[8];
+// block, four codes per word, into W[kW .. kW+7] (the word order of the P
+// buffer's TMEM columns).  `fast` (warp-uniform) says |m| < 2^22, so that the
+// ExpCast codes need no clip: m is the block's final reference max, so every
+// score satisfies s c <= m + 8.
+template <bool kExpcast, int kOff, int kW>
+__device__ __forceinline__ void codes32(const uint32_t (&X)[kCols], float c, float m, bool fast, uint32_t one,
+                                        uint32_t (&W)[32]) {
     if constexpr (kExpcast) {
         // t / 256 = fma(S, 8c / 256, (55.65 - 8m) / 256), both scalings exact
         const float c8s = __fmul_rn(c, 1.0f / 32.0f);
@@ -140,13 +140,13 @@ __device__ __forceinline__ void write_codes32(const uint32_t (&X)[kCols], float 
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const uint32_t sv[4] = {X[kOff + 4 * q], X[kOff + 4 * q + 1], X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]};
-                w[q] = expcast4<false>(sv, c8s, bs, one);
+                W[kW + q] = expcast4<false>(sv, c8s, bs, one);
             }
         } else {
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const uint32_t sv[4] = {X[kOff + 4 * q], X[kOff + 4 * q + 1], X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]};
-                w[q] = expcast4<true>(sv, c8s, bs, one);
+                W[kW + q] = expcast4<true>(sv, c8s, bs, one);
             }
         }
     } else {
@@ -155,12 +155,9 @@ __device__ __forceinline__ void write_codes32(const uint32_t (&X)[kCols], float 
         const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
 #pragma unroll
         for (int q = 0; q < 8; ++q)
-            w[q] = expconv4(pk2(X[kOff + 4 * q], X[kOff + 4 * q + 1]), pk2(X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]),
-                            cx2, nx2);
+            W[kW + q] = expconv4(pk2(X[kOff + 4 * q], X[kOff + 4 * q + 1]), pk2(X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]),
+                                 cx2, nx2);
     }
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(tp), "r"(w[0]),
-                 "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
-                 : "memory");
 }
 
 // Operands of the mean-restore MMA for blocks b0 .. b0+15 (row / channel
@@ -411,33 +408,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
+            // all 128 codes into registers: columns 64..127 from X while
+            // columns 0..63 are reloaded behind them
+            const uint32_t tp = tl + kTmemP0 + 32 * sb;
+            const bool fast = __all_sync(0xffffffffu, fabsf(m_new) < kExpcastFastMax);
+            uint32_t W[32];
+            codes32<kExpcast, 0, 16>(X, c, m_new, fast, p.one, W);
+            VCA_TMEM_LD32(tS, X);
+            codes32<kExpcast, 32, 24>(X, c, m_new, fast, p.one, W);
+            VCA_TMEM_LD32(tS + 32, (X + 32));
+            tmem_ld_wait();
+            // S(b) is read: QK(b+2) may overwrite the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.s_free + sb);
+            codes32<kExpcast, 0, 0>(X, c, m_new, fast, p.one, W);
+            codes32<kExpcast, 32, 8>(X, c, m_new, fast, p.one, W);
             // P buffer b&1 and row-sum slot b&1 are free once PV(b-2) completed
             if (b >= 2) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + sb, ((b - 2) >> 1) & 1, abort_flag, p.limit_ns));
             if (ok) {
                 tc_fence_after();
-                const uint32_t tp = tl + kTmemP0 + 32 * sb;
-                const bool fast = __all_sync(0xffffffffu, fabsf(m_new) < kExpcastFastMax);
-                // codes of columns 64..127 from X, reloading columns 0..63 behind them
-                write_codes32<kExpcast, 0>(X, c, m_new, fast, tp + 16, p.one);
-                VCA_TMEM_LD32(tS, X);
-                write_codes32<kExpcast, 32>(X, c, m_new, fast, tp + 24, p.one);
-                VCA_TMEM_LD32(tS + 32, (X + 32));
-                // block b-2's row sum from the slot of this parity
+                // block b-2's row sum from the slot of this parity, then P(b) and
+                // the cleared slot for PV(b) (PV(0) initialises E0)
                 const uint32_t te = tl + (sb == 0 ? kTmemE0 : kTmemE1);
                 uint32_t rs_raw = 0;
-                if (b >= 2) asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
-                tmem_ld_wait();
-                // S(b) is read: QK(b+2) may overwrite the buffer
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B.s_free + sb);
-                // clear the slot for PV(b) (PV(0) initialises E0); completes before P(b) is released
+                if (b >= 2) {
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
+                    tmem_ld_wait();
+                }
+                VCA_TMEM_ST32(tp, W);
                 if (b >= 1)
                     asm volatile(
                         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
                         ::"r"(te), "r"(0u) : "memory");
-                write_codes32<kExpcast, 0>(X, c, m_new, fast, tp, p.one);
-                write_codes32<kExpcast, 32>(X, c, m_new, fast, tp + 8, p.one);
                 if (b >= 2) {
                     // block b-2's sum, taken against m (this thread's max after b-2)
                     const float rs = __uint_as_float(rs_raw);
