@@ -114,10 +114,24 @@ __device__ __forceinline__ uint32_t e4m3_f16x2_splat(uint32_t code) {
     return h | (h << 16);
 }
 
-// Two E2M1 nibbles of a byte -> f16x2 (the low nibble in the low half).
-__device__ __forceinline__ uint32_t e2m1x2_f16x2(uint32_t byte) {
-    const __half2_raw h = __nv_cvt_fp4x2_to_halfraw2(static_cast<__nv_fp4x2_storage_t>(byte & 0xFFu), __NV_E2M1);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+// The four bytes of w, each two E2M1 nibbles -> f16x2 (the low nibble in the
+// low half): d[i] from byte i.
+__device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t &d0, uint32_t &d1, uint32_t &d2, uint32_t &d3) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
+        : "r"(w));
+}
+
+// (lo, hi) rounded to E2M1 (nearest even, saturating at 6) and decoded back,
+// as f16x2 (lo in the low half).
+__device__ __forceinline__ uint32_t e2m1_round_f16x2(float lo, float hi) {
+    uint32_t d;
+    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+        : "=r"(d)
+        : "f"(lo), "f"(hi));
+    return d;
 }
 
 // NVFP4 P of this thread's kCols keys against the reference max m: per group
@@ -153,9 +167,13 @@ __device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], float c, flo
         const uint32_t sf = e4m3x2(q1, 0.0f) & 0xFFu;
         const float inv = sRcp[sf];
         const uint32_t sf2 = sSf2[sf];
+        const uint64_t inv2 = pk2(__float_as_uint(inv), __float_as_uint(inv));
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-            P[8 * g + q] = f16x2_mul(e2m1x2_f16x2(e2m1x2(__fmul_rn(pv[2 * q], inv), __fmul_rn(pv[2 * q + 1], inv))), sf2);
+        for (int q = 0; q < 8; ++q) {
+            float x0, x1;
+            upk2(mul2(pk2(__float_as_uint(pv[2 * q]), __float_as_uint(pv[2 * q + 1])), inv2), x0, x1);
+            P[8 * g + q] = f16x2_mul(e2m1_round_f16x2(x0, x1), sf2);
+        }
     }
 }
 
@@ -303,10 +321,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int h = 0; h < 2; ++h) {
                         const uint32_t w = code[2 * g + h];   // keys 16g + 8h .. +7
                         uint4 o;
-                        o.x = f16x2_mul(e2m1x2_f16x2(w), sf2);
-                        o.y = f16x2_mul(e2m1x2_f16x2(w >> 8), sf2);
-                        o.z = f16x2_mul(e2m1x2_f16x2(w >> 16), sf2);
-                        o.w = f16x2_mul(e2m1x2_f16x2(w >> 24), sf2);
+                        e2m1x8_f16x2(w, o.x, o.y, o.z, o.w);
+                        o.x = f16x2_mul(o.x, sf2);
+                        o.y = f16x2_mul(o.y, sf2);
+                        o.z = f16x2_mul(o.z, sf2);
+                        o.w = f16x2_mul(o.w, sf2);
                         const int panel = g >> 2, chunk = (2 * g + h) & 7;
                         *reinterpret_cast<uint4 *>(vs + panel * kPanelBytes + sw128_offset(kOnesRows + t, chunk)) = o;
                     }

@@ -425,6 +425,13 @@ __device__ __forceinline__ uint32_t expcast4(const uint32_t (&s)[4], float c8s, 
     return w & prmt(t, 0u, 0xBA98);
 }
 
+// Two fp32 products, each rounded to nearest even (one packed instruction).
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
