@@ -121,7 +121,7 @@ __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_
     float a[4];
     upk2(fma2(s01, cx2, negmx2), a[0], a[1]);
     upk2(fma2(s23, cx2, negmx2), a[2], a[3]);
-    return e4m3x2(ex2_approx(a[0]), ex2_approx(a[1])) | (e4m3x2(ex2_approx(a[2]), ex2_approx(a[3])) << 16);
+    return e4m3x4(ex2_approx(a[0]), ex2_approx(a[1]), ex2_approx(a[2]), ex2_approx(a[3]));
 }
 
 // P codes of 32 keys (X[kOff .. kOff+31]) against the reference max m of the

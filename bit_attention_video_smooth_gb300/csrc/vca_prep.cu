@@ -73,11 +73,10 @@ __device__ __forceinline__ void quant_qk_block(const uint16_t *__restrict__ X, i
         uint32_t packed[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            const uint32_t a = e4m3x2(__fmul_rn(__uint_as_float(w[2 * j] << 16), inv),
-                                      __fmul_rn(__uint_as_float(w[2 * j] & 0xFFFF0000u), inv));
-            const uint32_t b = e4m3x2(__fmul_rn(__uint_as_float(w[2 * j + 1] << 16), inv),
-                                      __fmul_rn(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), inv));
-            packed[j] = a | (b << 16);
+            packed[j] = e4m3x4(__fmul_rn(__uint_as_float(w[2 * j] << 16), inv),
+                               __fmul_rn(__uint_as_float(w[2 * j] & 0xFFFF0000u), inv),
+                               __fmul_rn(__uint_as_float(w[2 * j + 1] << 16), inv),
+                               __fmul_rn(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), inv));
         }
         *reinterpret_cast<uint2 *>(out + static_cast<int64_t>(u) * 8) = make_uint2(packed[0], packed[1]);
     }
@@ -242,7 +241,7 @@ __global__ void __launch_bounds__(kThreads) prep_vquant_kernel(const uint16_t *_
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                     r[q] = __fmul_rn(__fsub_rn(bf16_bits_to_f32(sV[(t0 + 4 * j + q) * kRowStride + ch]), muf), iv);
-                w[j] = e4m3x2(r[0], r[1]) | (e4m3x2(r[2], r[3]) << 16);
+                w[j] = e4m3x4(r[0], r[1], r[2], r[3]);
             }
             *reinterpret_cast<uint4 *>(v_res + cb * kBlk + t0) = make_uint4(w[0], w[1], w[2], w[3]);
         }
