@@ -358,6 +358,21 @@ __device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
     return static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest));
 }
 
+// Eight fp32 values -> eight E2M1 codes in one word (value i in nibble i;
+// round to nearest even, saturate to 6): four cvt instructions and a pack.
+__device__ __forceinline__ uint32_t e2m1x8(const float (&v)[8]) {
+    uint32_t w;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(w)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+    return w;
+}
+
 // Value of an E4M3 byte (exact in fp32).
 __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
     __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3);

@@ -261,11 +261,15 @@ __global__ void __launch_bounds__(kThreads) prep_vquant_kernel(const uint16_t *_
             const uint32_t sf = e4m3(__fdiv_rn(a16, g6));
             float iv = 0.0f;
             if (sf != 0) iv = __fdiv_rn(1.0f, __fmul_rn(e4m3_to_f32(sf), gs));
-            uint32_t w[2] = {0u, 0u};
+            uint32_t w[2];
+            const uint64_t iv2 = pk2(__float_as_uint(iv), __float_as_uint(iv));
 #pragma unroll
-            for (int q = 0; q < 16; q += 2) {
-                const uint32_t byte = e2m1x2(__fmul_rn(r[q], iv), __fmul_rn(r[q + 1], iv)) & 0xFFu;
-                w[q >> 3] |= byte << (8 * ((q >> 1) & 3));
+            for (int h = 0; h < 2; ++h) {
+                float x[8];
+#pragma unroll
+                for (int q = 0; q < 8; q += 2)
+                    upk2(mul2(pk2(__float_as_uint(r[8 * h + q]), __float_as_uint(r[8 * h + q + 1])), iv2), x[q], x[q + 1]);
+                w[h] = e2m1x8(x);
             }
             *reinterpret_cast<uint2 *>(v_res + cb * (kBlk / 2) + t0 / 2) = make_uint2(w[0], w[1]);
             v_sf[cb * (kBlk / 16) + t0 / 16] = static_cast<uint8_t>(sf);
