@@ -186,9 +186,12 @@ def _prepped_both(V, orc, BH, N, seed, vmode=0):
     return ref, p
 
 
+# N spans one block, two, a ragged few (odd), the longest tail without a
+# mean-restore MMA (19 blocks), the first MMA on the last block (20), two
+# MMAs (32), and a later MMA on the last block (36)
 @pytest.mark.parametrize("expcast", [1, 0])
 @pytest.mark.parametrize("BH,N,seed", [(2, 1024, 0), (1, 128, 1), (1, 256, 5), (3, 384, 2), (2, 640, 6), (1, 2304, 3),
-                                        (2, 4096, 4)])
+                                        (1, 2432, 7), (1, 2560, 8), (2, 4096, 4), (1, 4608, 9)])
 def test_attention_parity_on_oracle_operands(V, orc, expcast, BH, N, seed):
     ref, p = _prepped_both(V, orc, BH, N, seed)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
