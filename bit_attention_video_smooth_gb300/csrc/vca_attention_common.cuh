@@ -18,14 +18,18 @@
 namespace vca {
 namespace attn {
 
-constexpr int kParts = 2;                  // softmax threads per query row (column halves)
-constexpr int kCols = kBlk / kParts;       // S columns per softmax thread
-constexpr int kSoftmaxWarps = 4 * kParts;  // two warps per TMEM lane quarter
+// Eight softmax warps, two per TMEM lane quarter.  The NVFP4 kernel splits a
+// row's S columns between the two (column halves); the 8-bit kernel gives
+// them alternate key blocks and holds a row in registers kCols columns at a
+// time.
+constexpr int kParts = 2;
+constexpr int kCols = kBlk / kParts;       // S columns held in registers at a time
+constexpr int kSoftmaxWarps = 4 * kParts;
 constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
 constexpr float kLazyTau = 8.0f;           // log2 units: the reference max moves by more than 2^8 only
 
 constexpr uint32_t kBarSoftmax = 1;        // all softmax warps
-constexpr uint32_t kBarPair0 = 2;          // + quarter: the two warps of one TMEM lane quarter
+constexpr uint32_t kBarPair0 = 2;          // + quarter: the two warps of one TMEM lane quarter (NVFP4 kernel)
 
 // Wait ignoring the abort flag (used only to drain work this thread issued).
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
