@@ -371,7 +371,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int b = par; b < nb; b += 2) {
             const int sb = b & 1;
             const float sk_b = sk_next;
-            if (b + 2 < nb) sk_next = skh[b + 2];
             const float c = __fmul_rn(__fmul_rn(sqv, sk_b), p.scale_log2);
             const uint32_t tS = tl + sb * 128;
             // the row max of S(b); X keeps columns 64..127
@@ -404,6 +403,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sMX[sb * kBlk + row] = valid ? m_new : __int_as_float(0x7fc00000);
                 bar_arrive_release(bar_out, 64);
             }
+            // the next block's key scale, loaded after the hand-over so that the
+            // fence before it never waits for this load
+            if (b + 2 < nb) sk_next = skh[b + 2];
             if (!__all_sync(0xffffffffu, valid)) {
                 ok = false;
                 break;
