@@ -9,7 +9,6 @@
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
-#include <cuda_fp4.h>
 
 namespace vca {
 
@@ -350,12 +349,6 @@ __device__ __forceinline__ uint32_t e4m3x4(float a, float b, float c, float d) {
 
 __device__ __forceinline__ uint32_t e4m3(float x) {
     return static_cast<uint32_t>(__nv_cvt_float_to_fp8(x, __NV_SATFINITE, __NV_E4M3));
-}
-
-// Two fp32 values -> two E2M1 nibbles (round to nearest even, saturate to 6);
-// `lo` lands in the low nibble.
-__device__ __forceinline__ uint32_t e2m1x2(float lo, float hi) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp4x2(make_float2(lo, hi), __NV_E2M1, cudaRoundNearest));
 }
 
 // Eight fp32 values -> eight E2M1 codes in one word (value i in nibble i;
