@@ -465,6 +465,36 @@ def table_line(w, peaks, reps: int = 3):
             vb = (v if order is None else v[order]).view(w.N // 128, 128, 128)
             res = vb - vb.mean(dim=1, keepdim=True)
             removed[key].append(1.0 - float((res * res).sum()) / total)
+    # permutation reuse (the pages group on a quarter of the steps and reuse
+    # the permutation over 4 adjacent ones): one group call and four prep +
+    # attention steps against the four steps alone, each schedule timed once
+    reuse = {}
+    for key, sched in (("four_steps_ms", ["prep", "attention"] * 4),
+                       ("group_and_four_steps_ms", ["group"] + ["prep", "attention"] * 4)):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for name in sched:
+            stages[name]()
+        e1.record()
+        torch.cuda.synchronize()
+        reuse[key] = e0.elapsed_time(e1)
+    reuse["group_overhead"] = reuse["group_and_four_steps_ms"] / reuse["four_steps_ms"] - 1.0
+    # ExpCast against exact softmax on sampled score rows of the first head:
+    # codes from the kernels' ExpCast arithmetic (the library's code entry, the
+    # reference max = the row max), decoded E4M3, renormalised; total
+    # variation per row
+    tv = None
+    if w.vmode == "e4m3":
+        s2 = (Qf[0, rows].double() @ Kf[0].double().T) * (1.4426950408889634 / 128 ** 0.5)
+        m2 = s2.max(dim=1, keepdim=True).values
+        s32 = s2.float().contiguous()
+        codes = torch.empty(s32.shape, dtype=torch.uint8, device="cuda")
+        vca.vca_expcast_codes(s32, torch.ones_like(s32), m2.float().expand_as(s32).contiguous(), codes)
+        ph = codes.view(torch.float8_e4m3fn).double()
+        ph = ph / ph.sum(dim=1, keepdim=True)
+        pe = torch.softmax(s2 * 0.6931471805599453, dim=1)
+        per_row = 0.5 * (ph - pe).abs().sum(dim=1)
+        tv = {"mean": float(per_row.mean()), "max": float(per_row.max()), "rows": int(per_row.numel())}
     peak, _ = attention_peak(w.vmode, peaks)
     hbm = (peaks or {}).get("hbm_gbs", 6800.0)
     gb, pb = group_bytes(w), prep_bytes(w)
@@ -477,6 +507,7 @@ def table_line(w, peaks, reps: int = 3):
         "prep_ms": ms["prep"], "prep_gbs": pb / ms["prep"] / 1e6, "prep_frac": pb / ms["prep"] / 1e6 / hbm,
         "hbm_peak_gbs": hbm, "rel_l2_vs_exact_attention": max(errs), "error_rows": "32 sampled rows x 2 heads",
         "energy_removed_by_block_means": {k: statistics.mean(v) for k, v in removed.items()},
+        "perm_reuse_4_steps": reuse, "expcast_tv_vs_softmax": tv,
     }
 
 
