@@ -465,6 +465,28 @@ def table_line(w, peaks, reps: int = 3):
             vb = (v if order is None else v[order]).view(w.N // 128, 128, 128)
             res = vb - vb.mean(dim=1, keepdim=True)
             removed[key].append(1.0 - float((res * res).sum()) / total)
+    # the QK Hadamard prep option: its prep time, and the error of attention over
+    # the rotated operands on the same sampled rows
+    p_h = vca.alloc_prep(w.B, w.H, w.N, vmode)
+    prep_h = lambda: vca.prep_quant(Q, K, V, g.perm, vmode, out=p_h, qk_hadamard=True)
+    for _ in range(2):
+        prep_h()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        prep_h()
+    e1.record()
+    torch.cuda.synchronize()
+    prep_h_ms = e0.elapsed_time(e1) / reps
+    O_h = vca.attention(p_h, w.B, w.H, w.N, expcast=w.expcast)
+    torch.cuda.synchronize()
+    errs_h = []
+    for h in (0, w.BH - 1):
+        s = (Qf[h, rows].double() @ Kf[h].double().T) / (128 ** 0.5)
+        ref = torch.softmax(s, dim=-1) @ Vf[h].double()
+        got = O_h.view(w.BH, w.N, 128)[h, rows].double()
+        errs_h.append(float(torch.linalg.norm(got - ref) / torch.linalg.norm(ref)))
+    del p_h, O_h
     # permutation reuse (the pages group on a quarter of the steps and reuse
     # the permutation over 4 adjacent ones): one group call and four prep +
     # attention steps against the four steps alone, each schedule timed once
@@ -508,6 +530,7 @@ def table_line(w, peaks, reps: int = 3):
         "hbm_peak_gbs": hbm, "rel_l2_vs_exact_attention": max(errs), "error_rows": "32 sampled rows x 2 heads",
         "energy_removed_by_block_means": {k: statistics.mean(v) for k, v in removed.items()},
         "perm_reuse_4_steps": reuse, "expcast_tv_vs_softmax": tv,
+        "qk_hadamard": {"prep_ms": prep_h_ms, "rel_l2_vs_exact_attention": max(errs_h)},
     }
 
 

@@ -69,15 +69,24 @@ int vca_group(const uint16_t *V, int B, int H, int N, int d, int k, int iters, i
 int vca_prep_quant(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int B, int H, int N,
                    int d, int vmode, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res, uint8_t *v_sf,
                    float *v_scale, uint16_t *v_mean, void *ws, size_t ws_bytes, void *stream) {
+    return vca_prep_quant_ex(Q, K, V, perm, B, H, N, d, vmode, 0u, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, ws,
+                             ws_bytes, stream);
+}
+
+int vca_prep_quant_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int B, int H,
+                      int N, int d, int vmode, uint32_t flags, uint8_t *q8, float *sq, uint8_t *k8, float *sk,
+                      uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean, void *ws, size_t ws_bytes,
+                      void *stream) {
     if (!shape_ok(B, H, N, d) || (vmode != VCA_V_E4M3 && vmode != VCA_V_NVFP4)) return VCA_ERR_INVALID_ARG;
+    if (flags & ~VCA_PREP_QK_HADAMARD) return VCA_ERR_INVALID_ARG;
     const void *ptrs[] = {Q, K, V, perm, q8, sq, k8, sk, v_res, v_scale, v_mean};
     for (const void *p : ptrs)
         if (!p || !aligned16(p)) return VCA_ERR_INVALID_ARG;
     if (vmode == VCA_V_NVFP4 && (!v_sf || !aligned16(v_sf))) return VCA_ERR_INVALID_ARG;
     const size_t need = vca_workspace_bytes(VCA_OP_PREP, B, H, N, d, 1, vmode);
     if (!ws || ws_bytes < need || !aligned16(ws)) return VCA_ERR_WORKSPACE;
-    return from_cuda(vca::launch_prep(Q, K, V, perm, B * H, N, vmode, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean,
-                                      ws, static_cast<cudaStream_t>(stream)));
+    return from_cuda(vca::launch_prep(Q, K, V, perm, B * H, N, vmode, flags, q8, sq, k8, sk, v_res, v_sf, v_scale,
+                                      v_mean, ws, static_cast<cudaStream_t>(stream)));
 }
 
 int vca_attention(const uint8_t *q8, const float *sq, const uint8_t *k8, const float *sk, const uint8_t *v_res,

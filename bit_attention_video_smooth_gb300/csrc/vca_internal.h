@@ -24,9 +24,10 @@ struct PrepWorkspace {
     size_t off_amax, off_inv, bytes;
 };
 PrepWorkspace prep_workspace_layout(int BH, int N);
+constexpr uint32_t kPrepQkHadamard = 1u;   // VCA_PREP_QK_HADAMARD
 cudaError_t launch_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int BH, int N,
-                        int vmode, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res, uint8_t *v_sf,
-                        float *v_scale, uint16_t *v_mean, void *ws, cudaStream_t st);
+                        int vmode, uint32_t flags, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res,
+                        uint8_t *v_sf, float *v_scale, uint16_t *v_mean, void *ws, cudaStream_t st);
 
 struct AttentionArgs {
     const uint8_t *q8, *k8, *v_res, *v_sf;

@@ -67,7 +67,7 @@ extern "C" int vca_prep_quant_noalloc(const uint16_t *Q, const uint16_t *K, cons
     if (vmode == VCA_V_NVFP4 && (!v_sf || !aligned16(v_sf))) return VCA_ERR_INVALID_ARG;
     void *ws = nullptr;
     if (scratch_for_current_device(&ws) != cudaSuccess) return VCA_ERR_CUDA;
-    const cudaError_t e = vca::launch_prep(Q, K, V, perm, B * H, N, vmode, q8, sq, k8, sk, v_res, v_sf, v_scale,
+    const cudaError_t e = vca::launch_prep(Q, K, V, perm, B * H, N, vmode, 0u, q8, sq, k8, sk, v_res, v_sf, v_scale,
                                            v_mean, ws, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? VCA_OK : VCA_ERR_CUDA;
 }

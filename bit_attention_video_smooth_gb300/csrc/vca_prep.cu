@@ -82,6 +82,72 @@ __device__ __forceinline__ void quant_qk_block(const uint16_t *__restrict__ X, i
     }
 }
 
+// The same block after rotating every row by the unnormalised 128-point
+// Walsh-Hadamard transform (the QK Hadamard option): fp32 butterflies in the
+// fixed order bit 0, 1, ..., 6 of the channel index, each pair (c, c + 2^k)
+// with bit k clear becoming (a + b, a - b).  A row's 128 channels sit in 16
+// consecutive lanes, 8 per lane: bits 0-2 are butterflied in registers, bits
+// 3-6 (the lane's bits 0-3) across lanes.  The stored scale is amax / 448
+// times `post` (a power of two: 1 for Q, 1/128 for K, so that sq sk q8 . k8
+// still approximates q . k).
+__device__ __forceinline__ void quant_qk_block_hadamard(const uint16_t *__restrict__ X, int64_t head_row0,
+                                                        const int32_t *__restrict__ rows, int row0, float post,
+                                                        uint8_t *__restrict__ out, float *__restrict__ scale,
+                                                        float *red) {
+    const int tid = threadIdx.x, lane = tid & 31;
+    float x[8][8];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int u = i * kThreads + tid;
+        const int r = u >> 4, c8 = (u & 15) * 8;
+        const int64_t src = head_row0 + (rows ? rows[r] : row0 + r);
+        const uint4 v = *reinterpret_cast<const uint4 *>(X + src * kD + c8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            x[i][2 * j] = __uint_as_float(w[j] << 16);
+            x[i][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int h = 1; h < 8; h <<= 1)
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                if (!(c & h)) {
+                    const float a = x[i][c], b = x[i][c + h];
+                    x[i][c] = __fadd_rn(a, b);
+                    x[i][c + h] = __fsub_rn(a, b);
+                }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            const bool upper = (lane >> m) & 1;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                const float y = __shfl_xor_sync(0xffffffffu, x[i][c], 1 << m);
+                x[i][c] = upper ? __fsub_rn(y, x[i][c]) : __fadd_rn(x[i][c], y);
+            }
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) amax = fmaxf(amax, fabsf(x[i][c]));
+    }
+    amax = block_max(amax, red);
+    float inv = 1.0f, s = 1.0f;
+    if (amax > 0.0f) {
+        inv = __fdiv_rn(448.0f, amax);
+        s = __fdiv_rn(amax, 448.0f);
+    }
+    if (tid == 0) *scale = __fmul_rn(s, post);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int u = i * kThreads + tid;
+        const uint32_t lo = e4m3x4(__fmul_rn(x[i][0], inv), __fmul_rn(x[i][1], inv), __fmul_rn(x[i][2], inv),
+                                   __fmul_rn(x[i][3], inv));
+        const uint32_t hi = e4m3x4(__fmul_rn(x[i][4], inv), __fmul_rn(x[i][5], inv), __fmul_rn(x[i][6], inv),
+                                   __fmul_rn(x[i][7], inv));
+        *reinterpret_cast<uint2 *>(out + static_cast<int64_t>(u) * 8) = make_uint2(lo, hi);
+    }
+}
+
 // Gather the block's 128 V rows into shared memory (token-major, padded rows)
 // as asynchronous 16-byte copies (cp.async): all of a thread's copies are in
 // flight at once, and the gather can run while the thread works on something
@@ -105,6 +171,7 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
+template <bool kHadamard>
 __global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__restrict__ Q,
                                                               const uint16_t *__restrict__ K,
                                                               const uint16_t *__restrict__ V,
@@ -123,8 +190,15 @@ __global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__
 
     // V's gather runs in the background while Q and K are quantised
     load_v_tile_async(V, head_row0, rows, sV);
-    quant_qk_block(Q, head_row0, nullptr, b * kBlk, q8 + blk_off, sq + static_cast<int64_t>(bh) * nb + b, red);
-    quant_qk_block(K, head_row0, rows, 0, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b, red);
+    if constexpr (kHadamard) {
+        quant_qk_block_hadamard(Q, head_row0, nullptr, b * kBlk, 1.0f, q8 + blk_off,
+                                sq + static_cast<int64_t>(bh) * nb + b, red);
+        quant_qk_block_hadamard(K, head_row0, rows, 0, 1.0f / kD, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b,
+                                red);
+    } else {
+        quant_qk_block(Q, head_row0, nullptr, b * kBlk, q8 + blk_off, sq + static_cast<int64_t>(bh) * nb + b, red);
+        quant_qk_block(K, head_row0, rows, 0, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b, red);
+    }
     cp_async_wait_all();
     __syncthreads();
 
@@ -290,14 +364,17 @@ PrepWorkspace prep_workspace_layout(int BH, int N) {
 }
 
 cudaError_t launch_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int BH, int N,
-                        int vmode, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res, uint8_t *v_sf,
-                        float *v_scale, uint16_t *v_mean, void *ws, cudaStream_t st) {
+                        int vmode, uint32_t flags, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res,
+                        uint8_t *v_sf, float *v_scale, uint16_t *v_mean, void *ws, cudaStream_t st) {
     const PrepWorkspace w = prep_workspace_layout(BH, N);
     unsigned char *base = static_cast<unsigned char *>(ws);
     float *amax = reinterpret_cast<float *>(base + w.off_amax);
     float *inv = reinterpret_cast<float *>(base + w.off_inv);
     const int nb = N / kBlk;
-    prep_stats_kernel<<<dim3(nb, BH), kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax);
+    if (flags & kPrepQkHadamard)
+        prep_stats_kernel<true><<<dim3(nb, BH), kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax);
+    else
+        prep_stats_kernel<false><<<dim3(nb, BH), kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     prep_scale_kernel<<<BH, kD, 0, st>>>(nb, vmode, amax, v_scale, inv);

@@ -25,7 +25,7 @@ VCA_OP_GROUP, VCA_OP_PREP, VCA_OP_ATTENTION = 0, 1, 2
 # Entry points declared in include/vca.h (the ABI test checks they are exported).
 EXPORTS = ("vca_status_string", "vca_version", "vca_workspace_bytes", "vca_group", "vca_prep_quant",
            "vca_attention", "vca_expcast_codes", "vca_e4m3_encode_bits", "vca_selftest_timeout",
-           "vca_set_wait_limit_ns", "vca_prep_quant_noalloc")
+           "vca_set_wait_limit_ns", "vca_prep_quant_noalloc", "vca_prep_quant_ex")
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"libvca.so is not built ({LIB_PATH}); run __graft_entry__.build() -- "
@@ -45,6 +45,8 @@ _SIGS = {
     "vca_selftest_timeout": (_I, [_P, ctypes.c_uint64, _P]),
     "vca_set_wait_limit_ns": (None, [ctypes.c_uint64]),
     "vca_prep_quant_noalloc": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "vca_prep_quant_ex": (_I, [_P, _P, _P, _P, _I, _I, _I, _I, _I, ctypes.c_uint32, _P, _P, _P, _P, _P, _P, _P, _P,
+                               _P, _SZ, _P]),
 }
 for _name, (_res, _args) in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -118,6 +120,18 @@ def vca_prep_quant(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_sf, v_sca
                              _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
                              _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
     _check(st, "vca_prep_quant")
+
+
+VCA_PREP_QK_HADAMARD = 1
+
+
+def vca_prep_quant_ex(Q, K, V, perm, vmode: int, flags: int, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, ws,
+                      stream=None) -> None:
+    B, H, N, d = Q.shape
+    st = _lib.vca_prep_quant_ex(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode, flags,
+                                _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
+                                _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    _check(st, "vca_prep_quant_ex")
 
 
 def vca_prep_quant_noalloc(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean,
@@ -216,10 +230,13 @@ def group(V: torch.Tensor, k: int, iters: int, out: Optional[Grouped] = None,
     return g
 
 
-def prep_quant(Q, K, V, perm, vmode=VCA_V_E4M3, out: Optional[Prepared] = None) -> Prepared:
+def prep_quant(Q, K, V, perm, vmode=VCA_V_E4M3, out: Optional[Prepared] = None,
+               qk_hadamard: bool = False) -> Prepared:
     B, H, N, _ = Q.shape
     p = out or alloc_prep(B, H, N, vmode, Q.device)
-    vca_prep_quant(Q, K, V, perm, vmode, p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean, p.ws)
+    flags = VCA_PREP_QK_HADAMARD if qk_hadamard else 0
+    vca_prep_quant_ex(Q, K, V, perm, vmode, flags, p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean,
+                      p.ws)
     return p
 
 

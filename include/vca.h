@@ -118,6 +118,27 @@ int vca_prep_quant(const uint16_t *Q, const uint16_t *K, const uint16_t *V, cons
                    void *ws, size_t ws_bytes, void *stream);
 
 /*
+ * vca_prep_quant_ex -- vca_prep_quant with option flags (flags = 0 is exactly
+ * vca_prep_quant; unknown bits return VCA_ERR_INVALID_ARG):
+ *   VCA_PREP_QK_HADAMARD  rotate every Q and K row by the unnormalised 128-point
+ *          Walsh-Hadamard transform H before the FP8 quantisation (the QK
+ *          Hadamard of the Q/K prior art the insight page discusses, which
+ *          spreads outlier channels over all channels).  H is symmetric with
+ *          H H = 128 I, so (H q) . (H k) = 128 q . k: sk carries the factor
+ *          1/128 (exact) and vca_attention needs no change.  The transform is
+ *          defined as fp32 butterflies in a fixed order -- for bit k = 0..6 of
+ *          the channel index, every pair (c, c + 2^k) with bit k of c clear
+ *          becomes (a + b, a - b) -- so its rounding is reproducible; then
+ *          s = amax / 448 and x8 = E4M3_rne_sat(x * (448 / amax)) as usual.
+ */
+#define VCA_PREP_QK_HADAMARD 1u
+int vca_prep_quant_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm,
+                      int B, int H, int N, int d, int vmode, uint32_t flags,
+                      uint8_t *q8, float *sq, uint8_t *k8, float *sk,
+                      uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean,
+                      void *ws, size_t ws_bytes, void *stream);
+
+/*
  * vca_prep_quant_noalloc -- the same computation and outputs as vca_prep_quant,
  * for callers that cannot pass the library any scratch device memory (a host
  * program that owns all device memory and gives an operator only its tensors,

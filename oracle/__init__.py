@@ -10,7 +10,8 @@ it with gcc on first use and wraps it for numpy arrays.  Each function cites the
 passage of the method it follows; see the C file for the readings taken where
 the pages are silent.
 
-Parity pins for every function are in ``tests/test_oracle_*.py``.
+Parity pins for every function are in ``tests/test_oracle_*.py`` (the QK
+Hadamard option of ``prep`` and ``fwht_f32`` in ``test_oracle_hadamard.py``).
 """
 from __future__ import annotations
 
@@ -70,6 +71,9 @@ def _load():
                 "orc_kmeans_sse": (ctypes.c_double, [P, i32, i32, P, P]),
                 "orc_prep": (i32, [P, P, P, P, i32, i32, i32, i32,
                                    P, P, P, P, P, P, P, P]),
+                "orc_prep_ex": (i32, [P, P, P, P, i32, i32, i32, i32, ctypes.c_uint,
+                                      P, P, P, P, P, P, P, P]),
+                "orc_fwht_f32": (None, [P, i32]),
                 "orc_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, f32, f32, i32, i32,
                                         P, i32, P, P]),
                 "orc_attention_exact": (i32, [P, P, P, i32, i32, i32, f32, P, i32, P]),
@@ -210,8 +214,27 @@ def group(V: np.ndarray, k: int, iters: int):
 # ---------------------------------------------------------------------------
 # Fused prep (paper page "method"; news page "V-Smooth" bullet "Demean")
 # ---------------------------------------------------------------------------
-def prep(Q, K, V, perm, vmode: int = V_E4M3) -> dict:
-    """Gather, block means, residual and Q/K quantisation for bf16 [BH,N,d]."""
+PREP_QK_HADAMARD = 1
+
+
+def fwht_f32(x) -> np.ndarray:
+    """Unnormalised Walsh-Hadamard transform of the last axis (a power of two)
+    as fp32 butterflies, bit 0 first (the rounding the device reproduces)."""
+    lib = _load()
+    a = np.array(x, dtype=np.float32, copy=True)
+    d = a.shape[-1]
+    flat = a.reshape(-1, d)
+    for r in range(flat.shape[0]):
+        row = np.ascontiguousarray(flat[r])
+        lib.orc_fwht_f32(_p(row), d)
+        flat[r] = row
+    return flat.reshape(a.shape)
+
+
+def prep(Q, K, V, perm, vmode: int = V_E4M3, qk_hadamard: bool = False) -> dict:
+    """Gather, block means, residual and Q/K quantisation for bf16 [BH,N,d].
+    qk_hadamard: rotate Q and K rows by fwht_f32 before the FP8 quantisation;
+    the key scales then carry the factor 1/d."""
     lib = _load()
     q, k, v = (_c(a, np.uint16) for a in (Q, K, V))
     pm = _c(perm, np.int32)
@@ -230,11 +253,12 @@ def prep(Q, K, V, perm, vmode: int = V_E4M3) -> dict:
         out["v_res"] = np.empty((BH, nb, d, BLK // 2), np.uint8)
         out["v_sf"] = np.empty((BH, nb, d, BLK // 16), np.uint8)
         out["v_scale"] = np.empty((BH,), np.float32)
-    rc = lib.orc_prep(_p(q), _p(k), _p(v), _p(pm), BH, N, d, vmode,
-                      _p(out["q8"]), _p(out["sq"]), _p(out["k8"]), _p(out["sk"]),
-                      _p(out["v_res"]), _p(out["v_sf"]), _p(out["v_scale"]), _p(out["v_mean"]))
+    flags = PREP_QK_HADAMARD if qk_hadamard else 0
+    rc = lib.orc_prep_ex(_p(q), _p(k), _p(v), _p(pm), BH, N, d, vmode, flags,
+                         _p(out["q8"]), _p(out["sq"]), _p(out["k8"]), _p(out["sk"]),
+                         _p(out["v_res"]), _p(out["v_sf"]), _p(out["v_scale"]), _p(out["v_mean"]))
     if rc:
-        raise ValueError("oracle prep: N must be a multiple of 128")
+        raise ValueError("oracle prep: N must be a multiple of 128 (and d a power of two with qk_hadamard)")
     return out
 
 

@@ -304,32 +304,66 @@ double orc_kmeans_sse(const uint16_t *V, int N, int d, const int32_t *labels, co
 /*          v_sf [BH][N/128][d][8] (one E4M3 scale per 16 tokens), v_scale [BH] */
 /* ------------------------------------------------------------------------- */
 
-/* Per-block absmax FP8 quantisation of one 128 x d tile (R8).  `rows` lists the
- * source rows (identity for Q, the permutation for K). */
-static void quant_qk_block(const uint16_t *X, const int32_t *rows, int d, uint8_t *out, float *scale)
+/* Walsh-Hadamard transform of x[0..d) (d a power of two), unnormalised
+ * (entries +-1), as fp32 butterflies in a fixed order: for bit k = 0, 1, ...
+ * every pair (c, c + 2^k) with bit k of c clear becomes (a + b, a - b).  The
+ * order fixes the rounding, so a device that follows it gets the same bits.
+ * H is symmetric with H H = d I, so (H q) . (H k) = d (q . k): rotating Q and
+ * K leaves QK^T unchanged up to the factor d, while spreading an outlier
+ * channel over all channels before the FP8 quantisation (the QK Hadamard of
+ * the Q/K prior art the insight page discusses). */
+void orc_fwht_f32(float *x, int d)
 {
-    float amax = 0.0f;
-    for (int i = 0; i < BLK; i++)
-        for (int x = 0; x < d; x++) {
-            float a = fabsf(orc_bf16_to_f32(X[(int64_t)rows[i] * d + x]));
-            if (a > amax) amax = a;
-        }
-    float inv = 1.0f, s = 1.0f;
-    if (amax > 0.0f) { inv = 448.0f / amax; s = amax / 448.0f; }
-    for (int i = 0; i < BLK; i++)
-        for (int x = 0; x < d; x++) {
-            float prod = orc_bf16_to_f32(X[(int64_t)rows[i] * d + x]) * inv;   /* one fp32 rounding */
-            out[(int64_t)i * d + x] = orc_e4m3_encode((double)prod);
-        }
-    *scale = s;
+    for (int h = 1; h < d; h <<= 1)
+        for (int c = 0; c < d; c++)
+            if (!(c & h)) {
+                float a = x[c], b = x[c + h];
+                x[c] = a + b;
+                x[c + h] = a - b;
+            }
 }
 
-int orc_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm,
-             int BH, int N, int d, int vmode,
-             uint8_t *q8, float *sq, uint8_t *k8, float *sk,
-             uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean)
+/* Per-block absmax FP8 quantisation of one 128 x d tile (R8).  `rows` lists the
+ * source rows (identity for Q, the permutation for K); with `hadamard` every
+ * row is first rotated by orc_fwht_f32.  The stored scale is amax / 448 times
+ * `post` (a power of two). */
+static void quant_qk_block(const uint16_t *X, const int32_t *rows, int d, int hadamard, float post, uint8_t *out,
+                           float *scale)
+{
+    float *t = malloc(sizeof(float) * (size_t)BLK * d);
+    for (int i = 0; i < BLK; i++) {
+        for (int x = 0; x < d; x++) t[(int64_t)i * d + x] = orc_bf16_to_f32(X[(int64_t)rows[i] * d + x]);
+        if (hadamard) orc_fwht_f32(t + (int64_t)i * d, d);
+    }
+    float amax = 0.0f;
+    for (int64_t i = 0; i < (int64_t)BLK * d; i++) {
+        float a = fabsf(t[i]);
+        if (a > amax) amax = a;
+    }
+    float inv = 1.0f, s = 1.0f;
+    if (amax > 0.0f) { inv = 448.0f / amax; s = amax / 448.0f; }
+    for (int64_t i = 0; i < (int64_t)BLK * d; i++) {
+        float prod = t[i] * inv;   /* one fp32 rounding */
+        out[i] = orc_e4m3_encode((double)prod);
+    }
+    *scale = s * post;
+    free(t);
+}
+
+/* flags: ORC_PREP_QK_HADAMARD rotates every Q and K row by the unnormalised
+ * Walsh-Hadamard transform before the FP8 quantisation; the key scale then
+ * carries the factor 1/d (exact, a power of two) so that sq sk q8 . k8 still
+ * approximates q . k. */
+int orc_prep_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm,
+                int BH, int N, int d, int vmode, unsigned flags,
+                uint8_t *q8, float *sq, uint8_t *k8, float *sk,
+                uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean)
 {
     if (N % BLK != 0 || d <= 0) return 1;
+    if (flags & ~1u) return 1;
+    const int had = (flags & 1u) != 0;
+    if (had && (d & (d - 1))) return 1;
+    const float kpost = had ? 1.0f / (float)d : 1.0f;
     const int nb = N / BLK;
     #pragma omp parallel for schedule(dynamic, 1)
     for (int bh = 0; bh < BH; bh++) {
@@ -341,8 +375,10 @@ int orc_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int3
         /* Q (original order) and K (permuted order) */
         for (int b = 0; b < nb; b++) {
             for (int i = 0; i < BLK; i++) ident[i] = b * BLK + i;
-            quant_qk_block(q, ident, d, q8 + ((int64_t)bh * N + (int64_t)b * BLK) * d, sq + (int64_t)bh * nb + b);
-            quant_qk_block(kk, pm + (int64_t)b * BLK, d, k8 + ((int64_t)bh * N + (int64_t)b * BLK) * d, sk + (int64_t)bh * nb + b);
+            quant_qk_block(q, ident, d, had, 1.0f, q8 + ((int64_t)bh * N + (int64_t)b * BLK) * d,
+                           sq + (int64_t)bh * nb + b);
+            quant_qk_block(kk, pm + (int64_t)b * BLK, d, had, kpost, k8 + ((int64_t)bh * N + (int64_t)b * BLK) * d,
+                           sk + (int64_t)bh * nb + b);
         }
         /* block means of the gathered V, and the residual against the rounded mean */
         for (int b = 0; b < nb; b++) {
@@ -401,6 +437,14 @@ int orc_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int3
         free(R);
     }
     return 0;
+}
+
+int orc_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm,
+             int BH, int N, int d, int vmode,
+             uint8_t *q8, float *sq, uint8_t *k8, float *sk,
+             uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean)
+{
+    return orc_prep_ex(Q, K, V, perm, BH, N, d, vmode, 0u, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -77,6 +77,12 @@ def test_invalid_arguments_rejected_without_cuda(lib):
                          None) == 1                                                                       # status
     lib.vca_selftest_timeout.argtypes = [P, ctypes.c_uint64, P]
     assert lib.vca_selftest_timeout(fake, 10, None) == 1
+    # prep option flags: only VCA_PREP_QK_HADAMARD (bit 0) is defined
+    lib.vca_prep_quant_ex.argtypes = [P, P, P, P] + [ctypes.c_int] * 5 + [ctypes.c_uint32] + [P] * 8 + \
+        [P, ctypes.c_size_t, P]
+    assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1024, 128, 0, 2, *([fake] * 8), fake, 1 << 30, None) == 1
+    assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1000, 128, 0, 1, *([fake] * 8), fake, 1 << 30, None) == 1
+    assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1024, 128, 0, 1, *([fake] * 8), None, 0, None) == 5
 
 
 def test_oracle_and_library_share_no_code():

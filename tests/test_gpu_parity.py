@@ -161,6 +161,31 @@ def test_prep_e4m3_parity(V, orc, BH, N, seed):
     np.testing.assert_allclose(p.v_scale.cpu().numpy(), ref["v_scale"], rtol=1e-6)
 
 
+@pytest.mark.parametrize("BH,N,seed", [(2, 1024, 10), (3, 384, 11), (1, 2432, 12)])
+def test_prep_qk_hadamard_parity(V, orc, BH, N, seed):
+    """The QK Hadamard option: the device's fp32 butterflies in the documented
+    order give the oracle's rotated rows bit for bit, so q8, k8, sq and sk
+    match exactly; the V outputs are those of the plain prep."""
+    q, k, v, perm = _prep_inputs(BH, N, seed)
+    q16, k16, v16 = (I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v))
+    ref = orc.prep(q16, k16, v16, perm.numpy(), qk_hadamard=True)
+    p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_E4M3, qk_hadamard=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(p.q8.cpu().numpy(), ref["q8"])
+    assert np.array_equal(p.k8.cpu().numpy(), ref["k8"])
+    assert np.array_equal(p.sq.cpu().numpy(), ref["sq"])
+    assert np.array_equal(p.sk.cpu().numpy(), ref["sk"])
+    plain = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_E4M3)
+    torch.cuda.synchronize()
+    assert torch.equal(plain.v_res, p.v_res) and torch.equal(plain.v_mean.view(torch.int16), p.v_mean.view(torch.int16))
+    # attention over the rotated operands against the oracle's, end to end
+    O = V.attention(p, 1, BH, N, expcast=True)
+    torch.cuda.synchronize()
+    O_ref = orc.attention(ref, orc.P_EXPCAST)
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(BH, N, 128), O_ref)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
 def test_prep_nvfp4_parity(V, orc):
     BH, N = 2, 1024
     q, k, v, perm = _prep_inputs(BH, N, 4)
