@@ -78,6 +78,25 @@ def test_sweep_prep_and_attention(V, orc, N):
     _check_prep_and_attention(V, orc, w, seed=41 + N % 97, heads=(w.BH // 2,), nrows=24)
 
 
+def test_fullsize_qk_hadamard_prep(V, orc):
+    """The QK Hadamard prep option at the Wan shape, in the launch configuration
+    of the full workload: the rotated and quantised Q and K of sampled heads
+    match the oracle bit for bit."""
+    w = I.WORKLOADS["wan"]
+    Q, K, Vv = I.make_qkv(w, seed=61, device="cuda")
+    perm = I.random_perm(w.BH, w.N, seed=62, device="cuda")
+    p = V.prep_quant(Q, K, Vv, perm, V.VCA_V_E4M3, qk_hadamard=True)
+    torch.cuda.synchronize()
+    Qf, Kf, Vf = (t.view(w.BH, w.N, 128) for t in (Q, K, Vv))
+    for h in (5, w.BH - 1):
+        ref = orc.prep(_u16(Qf[h])[None], _u16(Kf[h])[None], _u16(Vf[h])[None], perm[h].cpu().numpy()[None],
+                       qk_hadamard=True)
+        assert np.array_equal(p.q8[h].cpu().numpy(), ref["q8"][0])
+        assert np.array_equal(p.k8[h].cpu().numpy(), ref["k8"][0])
+        assert np.array_equal(p.sq[h].cpu().numpy(), ref["sq"][0])
+        assert np.array_equal(p.sk[h].cpu().numpy(), ref["sk"][0])
+
+
 def test_fullsize_group_sampled_heads(V, orc):
     """k-means at the Wan shape on sampled heads.
 
