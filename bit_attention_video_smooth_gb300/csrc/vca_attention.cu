@@ -129,6 +129,16 @@ __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_
 // buffer's TMEM columns).  `fast` (warp-uniform) says |m| < 2^22, so that the
 // ExpCast codes need no clip: m is the block's final reference max, so every
 // score satisfies s c <= m + 8.
+// The clipped ExpCast codes of 32 scores (taken only when |m| >= 2^22, i.e.
+// never for finite attention inputs of any realistic scale): out of line, so
+// the hot loop holds one copy of the code arithmetic per call site.
+__device__ __noinline__ void expcast32_clip(const uint32_t *sv, float c8s, float bs, uint32_t one, uint32_t *w) {
+    for (int q = 0; q < 8; ++q) {
+        const uint32_t s4[4] = {sv[4 * q], sv[4 * q + 1], sv[4 * q + 2], sv[4 * q + 3]};
+        w[q] = expcast4<true>(s4, c8s, bs, one);
+    }
+}
+
 template <bool kExpcast, int kOff, int kW>
 __device__ __forceinline__ void codes32(const uint32_t (&X)[kCols], float c, float m, bool fast, uint32_t one,
                                         uint32_t (&W)[32]) {
@@ -143,11 +153,13 @@ __device__ __forceinline__ void codes32(const uint32_t (&X)[kCols], float c, flo
                 W[kW + q] = expcast4<false>(sv, c8s, bs, one);
             }
         } else {
+            // copies, so that X and W themselves never need an address
+            uint32_t sv[32], w[8];
 #pragma unroll
-            for (int q = 0; q < 8; ++q) {
-                const uint32_t sv[4] = {X[kOff + 4 * q], X[kOff + 4 * q + 1], X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]};
-                W[kW + q] = expcast4<true>(sv, c8s, bs, one);
-            }
+            for (int e = 0; e < 32; ++e) sv[e] = X[kOff + e];
+            expcast32_clip(sv, c8s, bs, one, w);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) W[kW + q] = w[q];
         }
     } else {
         const float negm = -m;
