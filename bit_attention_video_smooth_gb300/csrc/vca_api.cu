@@ -16,7 +16,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 bool shape_ok(int B, int H, int N, int d) {
     if (B < 1 || H < 1 || N < 128 || d != 128 || (N % 128) != 0) return false;
     const int64_t BH = static_cast<int64_t>(B) * H;
-    return BH <= (1 << 20) && BH * N <= (static_cast<int64_t>(1) << 31) - 1;
+    return BH <= 65535 && BH * N <= (static_cast<int64_t>(1) << 31) - 1;   // BH is a grid y extent
 }
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? VCA_OK : VCA_ERR_CUDA; }

@@ -35,6 +35,10 @@
  *               v_scale fp32 [BH] (the per-(b,h) scale above the E4M3 scales)
  *   O             bf16 [B][H][N][d], rows in the original query order
  *
+ * Sizes accepted by every entry point: B >= 1, H >= 1, B*H <= 65,535 (one grid
+ * row of CTAs per head), N a positive multiple of 128, B*H*N <= 2^31 - 1
+ * tokens, d = 128.  Anything else is VCA_ERR_INVALID_ARG.
+ *
  * Return value: a vca_status.  Invalid arguments are reported synchronously and
  * launch nothing.  Device-side failures (a bounded wait that ran out) are
  * written to the optional `dev_status` word, which the caller reads after the
@@ -86,7 +90,7 @@ size_t vca_workspace_bytes(int op, int B, int H, int N, int d, int k, int vmode)
  * split into bf16 hi + lo parts (fp32 accumulation): labels equal those of an
  * exact computation except where two centroids are within ~2^-16 relative of
  * each other.
- * Requires N % 128 == 0, d == 128, 1 <= k <= min(N, 128), iters >= 1,
+ * Requires 1 <= k <= min(N, 128), 1 <= iters <= 1000,
  * ws_bytes >= vca_workspace_bytes(VCA_OP_GROUP, ...).
  * dev_status (optional, device int32): set to VCA_ERR_TIMEOUT if a bounded
  * wait inside the kernels ran out; left untouched otherwise.

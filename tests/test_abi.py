@@ -53,6 +53,11 @@ def test_workspace_sizes(lib):
     assert ws(0, 1, 2, 1024, 128, 0, 0) == 0        # k < 1
     assert ws(0, 1, 2, 1024, 128, 129, 0) == 0      # k above the supported maximum
     assert ws(2, 1, 2, 1024, 128, 8, 0) == 0        # attention needs no workspace
+    assert ws(0, 1, 65535, 128, 128, 8, 0) > 0      # B*H at the grid limit
+    assert ws(0, 256, 256, 128, 128, 8, 0) == 0     # B*H = 65,536: one past it
+    assert ws(0, 1, 16, 1 << 27, 128, 8, 0) == 0    # B*H*N = 2^31 tokens
+    assert ws(0, 0, 2, 1024, 128, 8, 0) == 0        # empty batch
+    assert ws(1, 1, 2, 0, 128, 8, 0) == 0           # empty sequence
 
 
 def test_invalid_arguments_rejected_without_cuda(lib):
@@ -65,6 +70,9 @@ def test_invalid_arguments_rejected_without_cuda(lib):
     assert lib.vca_attention(*([fake] * 8), 1, 2, 1000, 128, 0.0, 1, 0, fake, None, None) == 1
     # misaligned pointer
     assert lib.vca_attention(P(0x10001), *([fake] * 7), 1, 2, 1024, 128, 0.0, 1, 0, fake, None, None) == 1
+    # B*H beyond the grid limit, and an empty sequence
+    assert lib.vca_attention(*([fake] * 8), 256, 256, 1024, 128, 0.0, 1, 0, fake, None, None) == 1
+    assert lib.vca_attention(*([fake] * 8), 1, 2, 0, 128, 0.0, 1, 0, fake, None, None) == 1
     # ExpCast has no NVFP4 counterpart
     assert lib.vca_attention(*([fake] * 8), 1, 2, 1024, 128, 0.0, 1, 1, fake, None, None) == 2
     lib.vca_group.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
