@@ -86,8 +86,30 @@ def _ptr(t: Optional[torch.Tensor]):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream=None):
-    s = stream if stream is not None else torch.cuda.current_stream()
+def _buffers(where: str, need) -> torch.device:
+    """The library sees plain pointers and cannot check what they point to, so
+    the binding does: every (name, tensor, bytes) entry with a tensor must be
+    contiguous and hold at least `bytes` bytes, and all of them must sit on one
+    CUDA device, which is returned.  Sizes are checked first, so a call with
+    host tensors of the right sizes fails only on the device check."""
+    need = [(n, t, b) for n, t, b in need if t is not None]
+    for name, t, nbytes in need:
+        if not t.is_contiguous():
+            raise ValueError(f"{where}: {name} must be contiguous")
+        have = t.numel() * t.element_size()
+        if have < nbytes:
+            raise ValueError(f"{where}: {name} holds {have} bytes, {nbytes} needed")
+    for name, t, _ in need:
+        if not t.is_cuda:
+            raise ValueError(f"{where}: {name} is not a CUDA tensor")
+    devs = {t.device for _, t, _ in need}
+    if len(devs) != 1:
+        raise ValueError(f"{where}: tensors on several devices {sorted(str(d) for d in devs)}")
+    return devs.pop()
+
+
+def _stream(stream=None, device=None):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
     return ctypes.c_void_p(s.cuda_stream)
 
 
@@ -107,30 +129,56 @@ def vca_group(V: torch.Tensor, k: int, iters: int, labels: torch.Tensor, perm: t
               counts: Optional[torch.Tensor], centroids: Optional[torch.Tensor], ws: torch.Tensor,
               dev_status: Optional[torch.Tensor] = None, stream=None) -> None:
     B, H, N, d = V.shape
-    st = _lib.vca_group(_ptr(_u16(V)), B, H, N, d, k, iters, _ptr(labels), _ptr(perm), _ptr(counts),
-                        _ptr(centroids), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
-                        _stream(stream))
+    tok = B * H * N
+    dev = _buffers("vca_group", [("V", V, 2 * tok * d), ("labels", labels, 4 * tok), ("perm", perm, 4 * tok),
+                                 ("counts", counts, 4 * B * H * k), ("centroids", centroids, 4 * B * H * k * d),
+                                 ("ws", ws, 0), ("dev_status", dev_status, 4)])
+    with torch.cuda.device(dev):
+        st = _lib.vca_group(_ptr(_u16(V)), B, H, N, d, k, iters, _ptr(labels), _ptr(perm), _ptr(counts),
+                            _ptr(centroids), _ptr(ws), ws.numel() * ws.element_size(), _ptr(dev_status),
+                            _stream(stream, dev))
     _check(st, "vca_group")
 
 
 def vca_prep_quant(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, ws,
                    stream=None) -> None:
     B, H, N, d = Q.shape
-    st = _lib.vca_prep_quant(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode,
-                             _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
-                             _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    dev = _prep_buffers("vca_prep_quant", B, H, N, d, vmode, Q, K, V, perm, q8, sq, k8, sk, v_res, v_sf, v_scale,
+                        v_mean, ws=ws)
+    with torch.cuda.device(dev):
+        st = _lib.vca_prep_quant(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode,
+                                 _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
+                                 _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream, dev))
     _check(st, "vca_prep_quant")
 
 
 VCA_PREP_QK_HADAMARD = 1
 
 
+def _prep_buffers(where, B, H, N, d, vmode, Q, K, V, perm, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean,
+                  O=None, ws=None, dev_status=None):
+    """Byte counts of the prep's inputs and outputs (the attention's operands)
+    at this size and V format, checked against the tensors given."""
+    BH, tok, nb = B * H, B * H * N, N // 128
+    fp4 = vmode == VCA_V_NVFP4
+    return _buffers(where, [
+        ("Q", Q, 2 * tok * d), ("K", K, 2 * tok * d), ("V", V, 2 * tok * d), ("perm", perm, 4 * tok),
+        ("q8", q8, tok * d), ("sq", sq, 4 * BH * nb), ("k8", k8, tok * d), ("sk", sk, 4 * BH * nb),
+        ("v_res", v_res, tok * d // 2 if fp4 else tok * d), ("v_sf", v_sf, tok * d // 16 if fp4 else 0),
+        ("v_scale", v_scale, 4 * BH if fp4 else 4 * BH * d), ("v_mean", v_mean, 2 * BH * nb * d),
+        ("O", O, 2 * tok * d), ("ws", ws, 0), ("dev_status", dev_status, 4)])
+
+
 def vca_prep_quant_ex(Q, K, V, perm, vmode: int, flags: int, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, ws,
                       stream=None) -> None:
     B, H, N, d = Q.shape
-    st = _lib.vca_prep_quant_ex(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode, flags,
-                                _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
-                                _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(), _stream(stream))
+    dev = _prep_buffers("vca_prep_quant_ex", B, H, N, d, vmode, Q, K, V, perm, q8, sq, k8, sk, v_res, v_sf,
+                        v_scale, v_mean, ws=ws)
+    with torch.cuda.device(dev):
+        st = _lib.vca_prep_quant_ex(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode,
+                                    flags, _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf),
+                                    _ptr(v_scale), _ptr(_u16(v_mean)), _ptr(ws), ws.numel() * ws.element_size(),
+                                    _stream(stream, dev))
     _check(st, "vca_prep_quant_ex")
 
 
@@ -140,32 +188,46 @@ def vca_prep_quant_noalloc(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_s
     into the library (for callers that cannot provide device scratch memory).
     Calls that overlap on the GPU share that buffer and must be ordered."""
     B, H, N, d = Q.shape
-    st = _lib.vca_prep_quant_noalloc(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d, vmode,
-                                     _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf),
-                                     _ptr(v_scale), _ptr(_u16(v_mean)), _stream(stream))
+    dev = _prep_buffers("vca_prep_quant_noalloc", B, H, N, d, vmode, Q, K, V, perm, q8, sq, k8, sk, v_res, v_sf,
+                        v_scale, v_mean)
+    with torch.cuda.device(dev):
+        st = _lib.vca_prep_quant_noalloc(_ptr(_u16(Q)), _ptr(_u16(K)), _ptr(_u16(V)), _ptr(perm), B, H, N, d,
+                                         vmode, _ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf),
+                                         _ptr(v_scale), _ptr(_u16(v_mean)), _stream(stream, dev))
     _check(st, "vca_prep_quant_noalloc")
 
 
 def vca_attention(q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean, B: int, H: int, N: int, d: int,
                   softmax_scale: float, expcast: int, vmode: int, O, dev_status=None, stream=None) -> None:
-    st = _lib.vca_attention(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
-                            _ptr(_u16(v_mean)), B, H, N, d, float(softmax_scale), int(expcast), int(vmode),
-                            _ptr(_u16(O)), _ptr(dev_status), _stream(stream))
+    dev = _prep_buffers("vca_attention", B, H, N, d, vmode, None, None, None, None, q8, sq, k8, sk, v_res, v_sf,
+                        v_scale, v_mean, O=O, dev_status=dev_status)
+    with torch.cuda.device(dev):
+        st = _lib.vca_attention(_ptr(q8), _ptr(sq), _ptr(k8), _ptr(sk), _ptr(v_res), _ptr(v_sf), _ptr(v_scale),
+                                _ptr(_u16(v_mean)), B, H, N, d, float(softmax_scale), int(expcast), int(vmode),
+                                _ptr(_u16(O)), _ptr(dev_status), _stream(stream, dev))
     _check(st, "vca_attention")
 
 
 def vca_expcast_codes(s_raw, c, m, out, stream=None) -> None:
-    _check(_lib.vca_expcast_codes(_ptr(s_raw), _ptr(c), _ptr(m), s_raw.numel(), _ptr(out), _stream(stream)),
-           "vca_expcast_codes")
+    n = s_raw.numel()
+    dev = _buffers("vca_expcast_codes", [("s_raw", s_raw, 4 * n), ("c", c, 4 * n), ("m", m, 4 * n), ("out", out, n)])
+    with torch.cuda.device(dev):
+        _check(_lib.vca_expcast_codes(_ptr(s_raw), _ptr(c), _ptr(m), n, _ptr(out), _stream(stream, dev)),
+               "vca_expcast_codes")
 
 
 def vca_e4m3_encode_bits(start: int, n: int, out, stream=None) -> None:
-    _check(_lib.vca_e4m3_encode_bits(ctypes.c_uint32(start), n, _ptr(out), _stream(stream)), "vca_e4m3_encode_bits")
+    dev = _buffers("vca_e4m3_encode_bits", [("out", out, n)])
+    with torch.cuda.device(dev):
+        _check(_lib.vca_e4m3_encode_bits(ctypes.c_uint32(start), n, _ptr(out), _stream(stream, dev)),
+               "vca_e4m3_encode_bits")
 
 
 def vca_selftest_timeout(dev_status, limit_ns: int, stream=None) -> None:
-    _check(_lib.vca_selftest_timeout(_ptr(dev_status), ctypes.c_uint64(limit_ns), _stream(stream)),
-           "vca_selftest_timeout")
+    dev = _buffers("vca_selftest_timeout", [("dev_status", dev_status, 4)])
+    with torch.cuda.device(dev):
+        _check(_lib.vca_selftest_timeout(_ptr(dev_status), ctypes.c_uint64(limit_ns), _stream(stream, dev)),
+               "vca_selftest_timeout")
 
 
 # ---------------------------------------------------------------------------
