@@ -18,3 +18,16 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def V():
+    """The CUDA library's binding, built first if its sources are newer (the
+    build is incremental); GPU tests skip where there is no CUDA device."""
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from bit_attention_video_smooth_gb300 import build
+    build.build()
+    from bit_attention_video_smooth_gb300 import vca
+    return vca

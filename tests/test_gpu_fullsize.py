@@ -21,14 +21,6 @@ REL_L2 = 1e-3
 MAX_ABS = 4e-3
 
 
-@pytest.fixture(scope="module")
-def V():
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    from bit_attention_video_smooth_gb300 import vca
-    return vca
-
-
 def _u16(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 

@@ -19,14 +19,6 @@ REL_L2 = 1e-3
 MAX_ABS = 4e-3
 
 
-@pytest.fixture(scope="module")
-def V():
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    from bit_attention_video_smooth_gb300 import vca
-    return vca
-
-
 def _f32(u16):
     return (np.asarray(u16, np.uint16).astype(np.uint32) << 16).view(np.float32)
 

@@ -18,14 +18,6 @@ from bit_attention_video_smooth_gb300 import inputs as I
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def V():
-    if not torch.cuda.is_available():
-        pytest.skip("no CUDA device")
-    from bit_attention_video_smooth_gb300 import vca
-    return vca
-
-
 def _outputs(p):
     outs = [p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_scale, p.v_mean.view(torch.int16)]
     if p.v_sf is not None:
