@@ -166,8 +166,8 @@ def oracle_sample(w, seed: int = 0):
     import oracle
     from bit_attention_video_smooth_gb300 import inputs as I
 
-    cores = os.cpu_count() or 1
     oracle.build()
+    cores = oracle.threads()
     heads = max(1, min(w.BH, cores))
     rows_per_head = 64
     sub = I.with_n(w, w.N, H=heads, B=1)

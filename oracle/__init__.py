@@ -56,6 +56,7 @@ def _load():
             P = ctypes.c_void_p
             i32, i64, f32 = ctypes.c_int, ctypes.c_int64, ctypes.c_float
             sig = {
+                "orc_threads": (ctypes.c_int, []),
                 "orc_e4m3_decode": (ctypes.c_double, [ctypes.c_uint8]),
                 "orc_e4m3_encode": (ctypes.c_uint8, [ctypes.c_double]),
                 "orc_e2m1_decode": (ctypes.c_double, [ctypes.c_uint8]),
@@ -92,6 +93,11 @@ def _p(a):
 
 def _c(a, dtype):
     return np.ascontiguousarray(a, dtype=dtype)
+
+
+def threads() -> int:
+    """Threads the oracle's parallel loops use in this process."""
+    return int(_load().orc_threads())
 
 
 # ---------------------------------------------------------------------------

@@ -38,6 +38,7 @@
  *   R13 softmax scale 1/sqrt(d) unless given.
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -49,6 +50,10 @@
 
 enum { ORC_P_EXPCAST = 0, ORC_P_EXP = 1, ORC_P_NVFP4 = 2, ORC_P_EXACT = 3 };
 enum { ORC_V_E4M3 = 0, ORC_V_NVFP4 = 1 };
+
+/* Threads the parallel loops below run on (OpenMP's limit for this process,
+ * e.g. OMP_NUM_THREADS); reported beside the oracle's timings. */
+int orc_threads(void) { return omp_get_max_threads(); }
 
 /* ------------------------------------------------------------------------- */
 /* Number formats (OCP 8-bit floating point and microscaling specifications). */

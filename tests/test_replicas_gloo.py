@@ -58,7 +58,7 @@ def test_reference_arm_under_torchrun_prints_one_line(tmp_path):
     cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", "--nproc-per-node", "2",
            "--master-addr", "127.0.0.1", "--master-port", str(port), os.path.join(ROOT, "bench.py"),
            "--impl", "reference", "--gpus", "2", "--workload", "tiny", "--steps", "1", "--warmup", "1"]
-    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="", OMP_NUM_THREADS="2")
     r = subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=280)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
@@ -66,4 +66,5 @@ def test_reference_arm_under_torchrun_prints_one_line(tmp_path):
     line = json.loads(lines[0])
     assert line["impl"] == "reference" and line["n_gpus"] == 2
     assert line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
+    assert line["cpu_baseline"]["cores"] == 2        # the threads the oracle actually ran on
     assert line["e2e"]["h2d_bytes_per_step"] == 0
