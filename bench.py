@@ -58,9 +58,18 @@ class ClockSampler:
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, device_index: int):
-        self.idx = device_index
+        self.idx = self.smi_id(device_index)
         self.proc = None
         self.lines = []
+
+    @staticmethod
+    def smi_id(device_index: int) -> str:
+        """nvidia-smi's name for CUDA device `device_index`: CUDA numbers the
+        devices CUDA_VISIBLE_DEVICES lists, nvidia-smi all of them."""
+        vis = [x.strip() for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+        if device_index < len(vis) and (vis[device_index].isdigit() or vis[device_index].startswith("GPU-")):
+            return vis[device_index]
+        return str(device_index)
 
     def __enter__(self):
         try:

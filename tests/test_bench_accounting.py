@@ -63,3 +63,27 @@ def test_traffic_scales_with_the_work_and_tracks_the_sources(bench, monkeypatch)
     # a capture of other sources is not reported
     monkeypatch.setattr(bench, "kernel_sources_sha", lambda files: "0" * 64)
     assert bench.attention_traffic(w) is None
+
+
+def test_clock_sampler_names_the_device_nvidia_smi_sees(bench, monkeypatch):
+    monkeypatch.delenv("CUDA_VISIBLE_DEVICES", raising=False)
+    assert bench.ClockSampler.smi_id(0) == "0"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "5,2")
+    assert bench.ClockSampler.smi_id(0) == "5" and bench.ClockSampler.smi_id(1) == "2"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "GPU-8f0c, 3")
+    assert bench.ClockSampler.smi_id(0) == "GPU-8f0c" and bench.ClockSampler.smi_id(1) == "3"
+    monkeypatch.setenv("CUDA_VISIBLE_DEVICES", "")
+    assert bench.ClockSampler.smi_id(0) == "0"
+
+
+def test_clock_summary_reasons_and_median(bench):
+    c = bench.ClockSampler.__new__(bench.ClockSampler)
+    c.lines = ["0, 2070, 2070, 900.1, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "0, 1950, 2070, 1400.0, 0x4, Not Active, Not Active, Not Active, Active",
+               "0, 2010, 2070, 1300.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+               "garbage line"]
+    s = c.summary()
+    assert s["sm_mhz"] == 2010 and s["sm_max_mhz"] == 2070 and s["samples"] == 3
+    assert s["reasons"] == ["sw_power_cap"]
+    c.lines = []
+    assert c.summary()["reasons"] == ["unsampled"]
