@@ -62,6 +62,27 @@ def test_kmeans_brute_force_tiny(orc, seed):
     assert np.array_equal(counts[0], np.bincount(lab, minlength=k))
 
 
+def test_kmeans_objective_hand_values(orc):
+    """The k-means objective the GPU group is compared by: a hand-summed case,
+    the objective at the optimal centroids of the brute-force case's labels,
+    and invariance under renumbering the clusters (centroid rows permuted with
+    the labels), which a wrong centroid index would break."""
+    v = _bf16(np.array([[1, 2], [3, 4], [0, 0], [5, -1]], np.float32))
+    lab = np.array([0, 0, 1, 1], np.int32)
+    cent = np.array([[2, 3], [0, 1]], np.float32)
+    # (1+1) + (1+1) + (0+1) + (25+4)
+    assert orc.kmeans_sse(v, lab, cent) == 34.0
+    assert orc.kmeans_sse(v, 1 - lab, cent[::-1].copy()) == 34.0
+    assert orc.kmeans_sse(v, lab, np.array([[2, 3], [2.5, -0.5]], np.float32)) == 4.0 + 13.0
+    rng = np.random.default_rng(3)
+    x = _bf16(rng.standard_normal((40, 16)).astype(np.float32))
+    xf = _f32(x).astype(np.float64)
+    lab = rng.integers(0, 5, 40).astype(np.int32)
+    means = np.stack([xf[lab == c].mean(0) for c in range(5)])
+    got = orc.kmeans_sse(x, lab, means.astype(np.float32))
+    assert abs(got - _sse(xf, lab, 5)) <= 1e-6 * got
+
+
 def test_kmeans_init_and_empty_cluster(orc):
     # k = N: every token is its own strided initial centroid; duplicate rows
     # leave one cluster empty and it keeps its previous centroid
