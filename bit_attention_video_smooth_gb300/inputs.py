@@ -131,13 +131,16 @@ def random_perm(BH: int, N: int, seed: int = 0, device="cpu") -> torch.Tensor:
 
 
 def sample_rows(N: int, n: int, seed: int = 0) -> torch.Tensor:
-    """n distinct query rows in [0, N) that always include the first and last
-    128-row blocks' first and last rows; int32, sorted."""
+    """min(n, N) distinct query rows in [0, N), n >= 4, that always include the
+    first and last 128-row blocks' first and last rows; the others are drawn
+    from the remaining rows.  int32, sorted."""
     g = _gen(seed, "cpu")
-    fixed = torch.tensor([0, 127, N - 128, N - 1], dtype=torch.int64)
-    rest = torch.randperm(N, generator=g)[: max(0, n - 4)]
-    rows = torch.unique(torch.cat([fixed, rest]))[:n]
-    return rows.to(torch.int32)
+    fixed = torch.unique(torch.tensor([0, 127, N - 128, N - 1], dtype=torch.int64))
+    free = torch.ones(N, dtype=torch.bool)
+    free[fixed] = False
+    others = torch.nonzero(free).flatten()
+    rest = others[torch.randperm(others.numel(), generator=g)[: max(0, n - fixed.numel())]]
+    return torch.sort(torch.cat([fixed, rest])).values.to(torch.int32)
 
 
 def to_u16(x: torch.Tensor):
