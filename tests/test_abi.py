@@ -104,3 +104,21 @@ def test_oracle_and_library_share_no_code():
         assert "oracle" not in text.lower(), f
     binding = open(os.path.join(ROOT, "bit_attention_video_smooth_gb300", "vca.py")).read()
     assert "import oracle" not in binding and "from oracle" not in binding
+
+
+def test_header_compiles_as_c_and_links(lib, tmp_path):
+    """A plain C99 program includes include/vca.h, links libvca.so and makes
+    the calls that need no GPU (tests/c/abi_consumer.c)."""
+    import shutil
+    import subprocess
+    if shutil.which("gcc") is None:
+        pytest.skip("no C compiler")
+    from bit_attention_video_smooth_gb300 import build
+    libdir = os.path.dirname(build.build())
+    exe = str(tmp_path / "abi_consumer")
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    os.path.join(ROOT, "tests", "c", "abi_consumer.c"), "-L", libdir, "-lvca",
+                    f"-Wl,-rpath,{libdir}", "-o", exe], check=True)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.count("ok  ") == 10
