@@ -117,7 +117,7 @@ def test_codes_stay_below_the_clip_on_the_fast_path():
     c = (2.0 ** rng.uniform(-12, 2, n)).astype(np.float32)
     lim = (m + np.float32(8.0)).astype(np.float32)
     s = (lim.astype(np.float64) / c.astype(np.float64)).astype(np.float32)
-    # walk s down until fp32(s c) <= lim, then take a few neighbours below
+    # the largest s with fp32(s c) <= lim: step s down while the product exceeds it
     for _ in range(4):
         over = (s * c) > lim
         s = np.where(over, np.nextafter(s, np.float32(-np.inf) * np.sign(c)), s)
