@@ -1,0 +1,115 @@
+"""The attention kernels' TMEM column plans and shared-memory layouts, read
+from their sources and checked on the CPU.
+
+Both kernels hold S0, S1, two row-sum slots E0/E1 around the accumulator O, P
+and Q in the 512 TMEM columns of one CTA.  The PV MMA of an even block writes
+N = 144 columns [E0 | O] and of an odd block [O | E1], so those pairs must be
+contiguous; nothing may overlap.  Shared-memory tiles read by the tensor core
+with the 128-byte swizzle start on 1024-byte boundaries, mbarriers on 8-byte
+ones, and the whole layout fits the 227 KB a CTA may use.
+"""
+import os
+import re
+
+import pytest
+
+CSRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "bit_attention_video_smooth_gb300",
+                    "csrc")
+
+
+def constants(*files):
+    """Namespace-level integer constexprs of the files, evaluated in order."""
+    env = {}
+    for f in files:
+        text = open(os.path.join(CSRC, f)).read()
+        for m in re.finditer(r"^constexpr\s+(?:int|uint32_t)\s+([^;]*);", text, flags=re.M):
+            for part in m.group(1).split(","):
+                name, _, expr = part.partition("=")
+                expr = re.sub(r"//.*", "", expr).replace("/", "//").strip()
+                try:
+                    env[name.strip()] = int(eval(expr, {"__builtins__": {}}, dict(env)))
+                except (NameError, SyntaxError):
+                    pass
+    return env
+
+
+def _disjoint(ranges, total):
+    spans = sorted(ranges.values())
+    for (a0, a1), (b0, b1) in zip(spans, spans[1:]):
+        assert a1 <= b0, ranges
+    assert spans[0][0] >= 0 and spans[-1][1] <= total, ranges
+
+
+@pytest.fixture(scope="module")
+def e4m3():
+    return constants("vca_device.cuh", "vca_attention_common.cuh", "vca_attention.cu")
+
+
+@pytest.fixture(scope="module")
+def nvfp4():
+    return constants("vca_device.cuh", "vca_attention_common.cuh", "vca_attention_fp4.cu")
+
+
+def test_e4m3_tmem_plan(e4m3):
+    c = e4m3
+    cols = {"S0": (0, 128), "S1": (128, 256), "E0": (c["kTmemE0"], c["kTmemE0"] + 16),
+            "O": (c["kTmemO"], c["kTmemO"] + 128), "E1": (c["kTmemE1"], c["kTmemE1"] + 16),
+            "P0": (c["kTmemP0"], c["kTmemP0"] + 32), "P1": (c["kTmemP0"] + 32, c["kTmemP0"] + 64),
+            "Q": (c["kTmemQ"], c["kTmemQ"] + 32)}
+    _disjoint(cols, c["kTmemCols"])
+    assert c["kTmemCols"] == 512
+    assert c["kTmemE0"] + 16 == c["kTmemO"] and c["kTmemO"] + 128 == c["kTmemE1"]     # [E0 | O], [O | E1]
+
+
+def test_e4m3_shared_memory_layout(e4m3):
+    c = e4m3
+    assert c["kThreads"] == 384 and c["kTileBytes"] == 16384
+    for s in range(c["kKStages"]):
+        assert (c["kOffK"] + s * c["kTileBytes"]) % 1024 == 0
+    for s in range(c["kVStages"]):
+        stage = c["kOffV"] + s * c["kVStageBytes"]
+        assert stage % 1024 == 0 and (stage + c["kOnesBytes"]) % 1024 == 0      # [ones ; V] and [V ; ones]
+    assert c["kOffMA"] % 1024 == 0 and c["kOffMB"] % 1024 == 0
+    assert c["kOffBar"] % 8 == 0
+    assert c["kSmemBytes"] <= 232448
+    # the regions follow one another without overlap
+    order = ["kOffK", "kOffV", "kOffMA", "kOffMB", "kOffRS", "kOffRSM", "kOffSV", "kOffMX", "kOffL", "kOffBar",
+             "kOffMisc"]
+    offs = [c[k] for k in order]
+    assert offs == sorted(offs)
+    assert c["kOffRSM"] - c["kOffRS"] == c["kRsSlots"] * 128 * 4
+    # one mbarrier each: q_full, K and V full/empty rings, s_full, s_free, p_full, pv_done, drain (two each)
+    assert c["kNumBars"] == 1 + 2 * c["kKStages"] + 2 * c["kVStages"] + 2 * 5
+
+
+def test_nvfp4_tmem_plan(nvfp4):
+    c = nvfp4
+    cols = {"S0": (0, 128), "S1": (128, 256), "E0": (c["kTmemE0"], c["kTmemE0"] + 16),
+            "O": (c["kTmemO"], c["kTmemO"] + 128), "E1": (c["kTmemE1"], c["kTmemE1"] + 16),
+            "P": (c["kTmemP"], c["kTmemP"] + 64), "Q": (c["kTmemQ"], c["kTmemQ"] + 32)}
+    _disjoint(cols, c["kTmemCols"])
+    assert c["kTmemE0"] + 16 == c["kTmemO"] and c["kTmemO"] + 128 == c["kTmemE1"]
+
+
+def test_nvfp4_shared_memory_layout(nvfp4):
+    c = nvfp4
+    assert c["kThreads"] == 384
+    for s in range(c["kVStages"]):
+        for panel in range(2):
+            assert (c["kOffV"] + s * c["kVStageBytes"] + panel * c["kPanelBytes"]) % 1024 == 0
+    assert c["kOffMA"] % 1024 == 0 and c["kOffMB"] % 1024 == 0
+    for s in range(c["kRawStages"]):
+        assert (c["kOffRaw"] + s * c["kRawStageBytes"]) % 16 == 0                 # bulk copy destinations
+    assert c["kOffBar"] % 8 == 0 and c["kSmemBytes"] <= 232448
+    order = ["kOffK", "kOffV", "kOffRaw", "kOffMA", "kOffMB", "kOffRS", "kOffSV", "kOffPM", "kOffL", "kOffRcp",
+             "kOffSf2", "kOffBar", "kOffMisc"]
+    offs = [c[k] for k in order]
+    assert offs == sorted(offs)
+
+
+def test_the_evaluator_reads_the_sources(e4m3, nvfp4):
+    """Guard against a silent parse failure: the constants the checks use exist
+    and have the values the kernels' comments state."""
+    assert e4m3["kBlk"] == 128 and e4m3["kD"] == 128 and e4m3["kMeanJ"] == 16 and e4m3["kRsSlots"] == 32
+    assert e4m3["kOnesBytes"] == 2048 and e4m3["kVStageBytes"] == 2048 + 16384 + 2048
+    assert nvfp4["kCodeBytes"] == 8192 and nvfp4["kSfBytes"] == 1024 and nvfp4["kPanelBytes"] == 160 * 128
