@@ -190,6 +190,52 @@ def test_prep_nvfp4_parity(V, orc):
     assert (p.v_res.cpu().numpy() == ref["v_res"]).mean() >= 0.9999
 
 
+def _degenerate_inputs(BH=2, N=384, seed=13):
+    """Seeded inputs with the degenerate cases the prep has to handle: an
+    all-zero Q block (scale 1, codes 0, a uniform softmax row), an all-zero
+    permuted K block, a permuted V block that is one constant vector (a zero
+    residual), and a V channel that is zero over a whole head (a zero
+    per-channel amax)."""
+    q, k, v, perm = _prep_inputs(BH, N, seed)
+    q, k, v = (t.view(BH, N, 128).clone() for t in (q, k, v))
+    q[0, 128:256] = 0
+    k[1, perm[1, 0:128].long()] = 0
+    v[0, perm[0, 256:384].long()] = v[0, 7].clone()
+    v[1, :, 5] = 0
+    shape = (1, BH, N, 128)
+    return q.view(shape), k.view(shape), v.view(shape), perm
+
+
+@pytest.mark.parametrize("vmode", [0, 1])
+def test_prep_and_attention_on_degenerate_inputs(V, orc, vmode):
+    BH, N = 2, 384
+    q, k, v, perm = _degenerate_inputs(BH, N)
+    ref = orc.prep(*(I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v)), perm.numpy(), vmode=vmode)
+    p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), vmode)
+    torch.cuda.synchronize()
+    for name in ("q8", "sq", "k8", "sk"):
+        assert np.array_equal(getattr(p, name).cpu().numpy(), ref[name]), name
+    assert p.sq.cpu().numpy()[0, 1] == 1.0 and p.sk.cpu().numpy()[1, 0] == 1.0     # the zero blocks
+    assert not p.q8.cpu().numpy()[0, 128:256].any()
+    vm = p.v_mean.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (vm == ref["v_mean"]).mean() >= 0.9999
+    assert (p.v_res.cpu().numpy() == ref["v_res"]).mean() >= 0.9999
+    assert not p.v_res.cpu().numpy()[0, 2].any()                                  # the constant block
+    if vmode == 0:
+        assert p.v_scale.cpu().numpy()[1, 5] == 1.0                               # the zero channel
+        np.testing.assert_allclose(p.v_scale.cpu().numpy(), ref["v_scale"], rtol=1e-6)
+    else:
+        assert not p.v_sf.cpu().numpy()[0, 2].any()
+        assert (p.v_sf.cpu().numpy() == ref["v_sf"]).mean() >= 0.9999
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    O = V.attention(p, 1, BH, N, expcast=(vmode == 0), dev_status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    O_ref = orc.attention(ref, orc.P_EXPCAST if vmode == 0 else orc.P_NVFP4)
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(BH, N, 128), O_ref)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
 # ---------------------------------------------------------------------------
 # attention
 # ---------------------------------------------------------------------------
