@@ -97,6 +97,39 @@ def test_group_bit_exact_on_separated_clusters(V, orc, BH, N, k, iters):
     np.testing.assert_allclose(g.centroids.cpu().numpy(), ref_cent, rtol=1e-5, atol=1e-5)
 
 
+def _degenerate_v(BH, N, case, seed=17):
+    """bf16 V [BH, N, 128]: every token the same vector per head ("constant"),
+    or two distinct vectors alternating in runs of 8 tokens ("two")."""
+    g = torch.Generator().manual_seed(seed)
+    a = torch.randn((BH, 1, 128), generator=g)
+    if case == "constant":
+        v = a.expand(BH, N, 128)
+    else:
+        b = torch.randn((BH, 1, 128), generator=g) * 4.0
+        pick = ((torch.arange(N) // 8) % 2 == 1).view(1, N, 1)
+        v = torch.where(pick, b, a)
+    return v.to(torch.bfloat16).contiguous()
+
+
+@pytest.mark.parametrize("case,k", [("constant", 8), ("two", 4), ("two", 64)])
+def test_group_on_degenerate_values(V, orc, case, k):
+    """Ties everywhere: with every token equal all distances tie and every
+    label is 0 (ties go to the lowest index; the other clusters stay empty and
+    keep their centroids); with two distinct tokens the labels follow the
+    initial centroids' copies of them, the lowest index among equal ones."""
+    BH, N, iters = 2, 512, 3
+    v16 = _degenerate_v(BH, N, case)
+    ref_lab, ref_perm, ref_cnt, ref_cent = orc.group(I.to_u16(v16), k, iters)
+    g = V.group(v16.view(1, BH, N, 128).cuda(), k, iters)
+    torch.cuda.synchronize()
+    assert np.array_equal(g.labels.cpu().numpy(), ref_lab)
+    assert np.array_equal(g.perm.cpu().numpy(), ref_perm)
+    assert np.array_equal(g.counts.cpu().numpy(), ref_cnt)
+    np.testing.assert_allclose(g.centroids.cpu().numpy(), ref_cent, rtol=1e-6, atol=1e-6)
+    if case == "constant":
+        assert not ref_lab.any() and np.array_equal(ref_perm, np.tile(np.arange(N), (BH, 1)))
+
+
 def _check_perm_properties(labels, perm, counts, k):
     BH, N = labels.shape
     for bh in range(BH):
