@@ -75,6 +75,7 @@ def _load():
                 "orc_prep_ex": (i32, [P, P, P, P, i32, i32, i32, i32, ctypes.c_uint,
                                       P, P, P, P, P, P, P, P]),
                 "orc_fwht_f32": (None, [P, i32]),
+                "orc_k_channel_mean": (None, [P, P, i32, i32, P]),
                 "orc_attention": (i32, [P, P, P, P, P, P, P, P, i32, i32, i32, f32, f32, i32, i32,
                                         P, i32, P, P]),
                 "orc_attention_exact": (i32, [P, P, P, i32, i32, i32, f32, P, i32, P]),
@@ -221,6 +222,23 @@ def group(V: np.ndarray, k: int, iters: int):
 # Fused prep (paper page "method"; news page "V-Smooth" bullet "Demean")
 # ---------------------------------------------------------------------------
 PREP_QK_HADAMARD = 1
+PREP_K_SMOOTH = 2
+
+
+def k_channel_mean(K, perm) -> np.ndarray:
+    """The channel mean of K over the sequence of each (b,h) that K smoothing
+    subtracts (fp32, a fixed summation order: a halving tree per permuted
+    128-token block, the block sums in block order, divided by N)."""
+    lib = _load()
+    k = _c(K, np.uint16)
+    pm = _c(perm, np.int32)
+    BH, N, d = k.shape
+    out = np.empty((BH, d), np.float32)
+    for bh in range(BH):
+        row = np.empty(d, np.float32)
+        lib.orc_k_channel_mean(_p(np.ascontiguousarray(k[bh])), _p(np.ascontiguousarray(pm[bh])), N, d, _p(row))
+        out[bh] = row
+    return out
 
 
 def fwht_f32(x) -> np.ndarray:
@@ -237,10 +255,11 @@ def fwht_f32(x) -> np.ndarray:
     return flat.reshape(a.shape)
 
 
-def prep(Q, K, V, perm, vmode: int = V_E4M3, qk_hadamard: bool = False) -> dict:
+def prep(Q, K, V, perm, vmode: int = V_E4M3, qk_hadamard: bool = False, k_smooth: bool = False) -> dict:
     """Gather, block means, residual and Q/K quantisation for bf16 [BH,N,d].
     qk_hadamard: rotate Q and K rows by fwht_f32 before the FP8 quantisation;
-    the key scales then carry the factor 1/d."""
+    the key scales then carry the factor 1/d.  k_smooth: subtract the keys'
+    channel mean (k_channel_mean) before that."""
     lib = _load()
     q, k, v = (_c(a, np.uint16) for a in (Q, K, V))
     pm = _c(perm, np.int32)
@@ -259,7 +278,7 @@ def prep(Q, K, V, perm, vmode: int = V_E4M3, qk_hadamard: bool = False) -> dict:
         out["v_res"] = np.empty((BH, nb, d, BLK // 2), np.uint8)
         out["v_sf"] = np.empty((BH, nb, d, BLK // 16), np.uint8)
         out["v_scale"] = np.empty((BH,), np.float32)
-    flags = PREP_QK_HADAMARD if qk_hadamard else 0
+    flags = (PREP_QK_HADAMARD if qk_hadamard else 0) | (PREP_K_SMOOTH if k_smooth else 0)
     rc = lib.orc_prep_ex(_p(q), _p(k), _p(v), _p(pm), BH, N, d, vmode, flags,
                          _p(out["q8"]), _p(out["sq"]), _p(out["k8"]), _p(out["sk"]),
                          _p(out["v_res"]), _p(out["v_sf"]), _p(out["v_scale"]), _p(out["v_mean"]))

@@ -329,15 +329,19 @@ void orc_fwht_f32(float *x, int d)
 }
 
 /* Per-block absmax FP8 quantisation of one 128 x d tile (R8).  `rows` lists the
- * source rows (identity for Q, the permutation for K); with `hadamard` every
- * row is first rotated by orc_fwht_f32.  The stored scale is amax / 448 times
- * `post` (a power of two). */
-static void quant_qk_block(const uint16_t *X, const int32_t *rows, int d, int hadamard, float post, uint8_t *out,
-                           float *scale)
+ * source rows (identity for Q, the permutation for K); with `shift` (K
+ * smoothing) every value first has its channel's shift subtracted in fp32;
+ * with `hadamard` every row is then rotated by orc_fwht_f32.  The stored
+ * scale is amax / 448 times `post` (a power of two). */
+static void quant_qk_block(const uint16_t *X, const int32_t *rows, int d, const float *shift, int hadamard,
+                           float post, uint8_t *out, float *scale)
 {
     float *t = malloc(sizeof(float) * (size_t)BLK * d);
     for (int i = 0; i < BLK; i++) {
-        for (int x = 0; x < d; x++) t[(int64_t)i * d + x] = orc_bf16_to_f32(X[(int64_t)rows[i] * d + x]);
+        for (int x = 0; x < d; x++) {
+            t[(int64_t)i * d + x] = orc_bf16_to_f32(X[(int64_t)rows[i] * d + x]);
+            if (shift) t[(int64_t)i * d + x] = t[(int64_t)i * d + x] - shift[x];   /* one fp32 rounding */
+        }
         if (hadamard) orc_fwht_f32(t + (int64_t)i * d, d);
     }
     float amax = 0.0f;
@@ -355,18 +359,51 @@ static void quant_qk_block(const uint16_t *X, const int32_t *rows, int d, int ha
     free(t);
 }
 
+/* K smoothing (SageAttention's treatment of the keys' channel bias): the
+ * channel mean of K over the whole sequence of one (b,h), subtracted from
+ * every key before the FP8 quantisation.  Every score of a query row then
+ * moves by the same q . mean, which softmax ignores.  The mean is a fixed
+ * fp32 computation, so that it can be reproduced exactly: per permuted
+ * 128-token block a halving tree (token i plus token i + 64 for i < 64, then
+ * i + 32, ..., i + 1), the block sums added in block order, the total divided
+ * by N. */
+static float tree_sum128(const float *x)
+{
+    float y[BLK];
+    for (int i = 0; i < BLK; i++) y[i] = x[i];
+    for (int h = BLK / 2; h >= 1; h >>= 1)
+        for (int i = 0; i < h; i++) y[i] = y[i] + y[i + h];
+    return y[0];
+}
+
+void orc_k_channel_mean(const uint16_t *K, const int32_t *perm, int N, int d, float *mean)
+{
+    const int nb = N / BLK;
+    float col[BLK];
+    for (int x = 0; x < d; x++) {
+        float total = 0.0f;
+        for (int b = 0; b < nb; b++) {
+            for (int i = 0; i < BLK; i++) col[i] = orc_bf16_to_f32(K[(int64_t)perm[b * BLK + i] * d + x]);
+            total = total + tree_sum128(col);
+        }
+        mean[x] = total / (float)N;
+    }
+}
+
 /* flags: ORC_PREP_QK_HADAMARD rotates every Q and K row by the unnormalised
  * Walsh-Hadamard transform before the FP8 quantisation; the key scale then
  * carries the factor 1/d (exact, a power of two) so that sq sk q8 . k8 still
- * approximates q . k. */
+ * approximates q . k.  ORC_PREP_K_SMOOTH subtracts the keys' channel mean
+ * (orc_k_channel_mean) first. */
 int orc_prep_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm,
                 int BH, int N, int d, int vmode, unsigned flags,
                 uint8_t *q8, float *sq, uint8_t *k8, float *sk,
                 uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean)
 {
     if (N % BLK != 0 || d <= 0) return 1;
-    if (flags & ~1u) return 1;
+    if (flags & ~3u) return 1;
     const int had = (flags & 1u) != 0;
+    const int ksmooth = (flags & 2u) != 0;
     if (had && (d & (d - 1))) return 1;
     const float kpost = had ? 1.0f / (float)d : 1.0f;
     const int nb = N / BLK;
@@ -377,14 +414,20 @@ int orc_prep_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const i
         int32_t ident[BLK];
         float *R = malloc(sizeof(float) * (size_t)N * d);   /* residual, permuted order [slot][ch] */
 
-        /* Q (original order) and K (permuted order) */
+        /* Q (original order) and K (permuted order, smoothed on request) */
+        float *kmean = NULL;
+        if (ksmooth) {
+            kmean = malloc(sizeof(float) * (size_t)d);
+            orc_k_channel_mean(kk, pm, N, d, kmean);
+        }
         for (int b = 0; b < nb; b++) {
             for (int i = 0; i < BLK; i++) ident[i] = b * BLK + i;
-            quant_qk_block(q, ident, d, had, 1.0f, q8 + ((int64_t)bh * N + (int64_t)b * BLK) * d,
+            quant_qk_block(q, ident, d, NULL, had, 1.0f, q8 + ((int64_t)bh * N + (int64_t)b * BLK) * d,
                            sq + (int64_t)bh * nb + b);
-            quant_qk_block(kk, pm + (int64_t)b * BLK, d, had, kpost, k8 + ((int64_t)bh * N + (int64_t)b * BLK) * d,
-                           sk + (int64_t)bh * nb + b);
+            quant_qk_block(kk, pm + (int64_t)b * BLK, d, kmean, had, kpost,
+                           k8 + ((int64_t)bh * N + (int64_t)b * BLK) * d, sk + (int64_t)bh * nb + b);
         }
+        free(kmean);
         /* block means of the gathered V, and the residual against the rounded mean */
         for (int b = 0; b < nb; b++) {
             for (int x = 0; x < d; x++) {
