@@ -151,8 +151,10 @@ int vca_prep_quant_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, c
  * Scratch: a buffer of VCA_NOALLOC_SCRATCH_BYTES built into the library, which
  * every GPU that loads the library holds until the process exits.  Problems
  * whose prep workspace (vca_workspace_bytes(VCA_OP_PREP, ...)) exceeds it return
- * VCA_ERR_WORKSPACE and launch nothing; 16 MiB covers B*H*(N/128) up to 32,640
- * blocks (B=1, H=40, N=70,656 needs 11.3 MB).  The first call on a device looks
+ * VCA_ERR_WORKSPACE and launch nothing.  That workspace is 512 bytes per
+ * 128-token block plus 512 bytes per head, so 16 MiB covers exactly the
+ * problems with B*H*(N/128) + B*H <= 32,768 (B=1, H=40, N=70,656 needs 22,120
+ * of those units, 11.3 MB).  The first call on a device looks
  * up the buffer's device address (make it before any stream capture).  Every
  * call shares the one buffer: calls that overlap on the GPU race and must be
  * ordered by the caller.  Nothing in the buffer needs clearing between calls.

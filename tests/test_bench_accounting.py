@@ -29,14 +29,20 @@ def test_attention_flops_of_the_wan_call():
 
 
 def test_peaks_from_the_measured_rates(bench):
-    peaks = {"bf16_tflops_sustained": 1701.9}
+    """The attention kernels run at full clock without the power cap: their
+    peaks come from the burst cuBLAS bf16 rate b (FP8 = 2 b by the nominal
+    ratio 4.5 / 2.25), never from the power-capped sustained figure."""
+    peaks = {"bf16_tflops": 1950.6, "bf16_tflops_sustained": 1717.9}
     fp8, src = bench.attention_peak("e4m3", peaks)
-    assert fp8 == pytest.approx(3403.8) and "measured" in src
+    assert fp8 == pytest.approx(3901.2) and "burst" in src
     fp4, _ = bench.attention_peak("nvfp4", peaks)
     # QK at the FP8 rate (2b), PV on f16 operands at b: 1 / (0.5 / 2b + 0.5 / b)
-    assert fp4 == pytest.approx(1.0 / (0.5 / 3403.8 + 0.5 / 1701.9))
+    assert fp4 == pytest.approx(1.0 / (0.5 / 3901.2 + 0.5 / 1950.6))
     fallback, src = bench.attention_peak("e4m3", None)
-    assert fallback == pytest.approx(3400.0) and "fallback" in src
+    assert fallback == pytest.approx(3800.0) and "fallback" in src
+    # against nominal dense rates: FP8 4.5 PF; the NVFP4 kernel's QK at FP8, PV at bf16
+    assert bench.attention_nominal("e4m3") == pytest.approx(4500.0)
+    assert bench.attention_nominal("nvfp4") == pytest.approx(1.0 / (0.5 / 4500.0 + 0.5 / 2250.0))
 
 
 def test_algorithmic_bytes(bench):
