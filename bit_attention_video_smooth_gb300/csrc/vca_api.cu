@@ -47,8 +47,9 @@ size_t vca_workspace_bytes(int op, int B, int H, int N, int d, int k, int vmode)
             if (k < 1 || k > vca::kMaxK || k > N) return 0;
             return vca::group_workspace_layout(BH, N, k).bytes;
         case VCA_OP_PREP:
+        case VCA_OP_PREP_KSMOOTH:
             if (vmode != VCA_V_E4M3 && vmode != VCA_V_NVFP4) return 0;
-            return vca::prep_workspace_layout(BH, N).bytes;
+            return vca::prep_workspace_layout(BH, N, op == VCA_OP_PREP_KSMOOTH ? vca::kPrepKSmooth : 0u).bytes;
         default:
             return 0;
     }
@@ -78,12 +79,13 @@ int vca_prep_quant_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, c
                       uint8_t *v_res, uint8_t *v_sf, float *v_scale, uint16_t *v_mean, void *ws, size_t ws_bytes,
                       void *stream) {
     if (!shape_ok(B, H, N, d) || (vmode != VCA_V_E4M3 && vmode != VCA_V_NVFP4)) return VCA_ERR_INVALID_ARG;
-    if (flags & ~VCA_PREP_QK_HADAMARD) return VCA_ERR_INVALID_ARG;
+    if (flags & ~(VCA_PREP_QK_HADAMARD | VCA_PREP_K_SMOOTH)) return VCA_ERR_INVALID_ARG;
     const void *ptrs[] = {Q, K, V, perm, q8, sq, k8, sk, v_res, v_scale, v_mean};
     for (const void *p : ptrs)
         if (!p || !aligned16(p)) return VCA_ERR_INVALID_ARG;
     if (vmode == VCA_V_NVFP4 && (!v_sf || !aligned16(v_sf))) return VCA_ERR_INVALID_ARG;
-    const size_t need = vca_workspace_bytes(VCA_OP_PREP, B, H, N, d, 1, vmode);
+    const size_t need = vca_workspace_bytes((flags & VCA_PREP_K_SMOOTH) ? VCA_OP_PREP_KSMOOTH : VCA_OP_PREP, B, H, N, d, 1,
+                                            vmode);
     if (!ws || ws_bytes < need || !aligned16(ws)) return VCA_ERR_WORKSPACE;
     return from_cuda(vca::launch_prep(Q, K, V, perm, B * H, N, vmode, flags, q8, sq, k8, sk, v_res, v_sf, v_scale,
                                       v_mean, ws, static_cast<cudaStream_t>(stream)));

@@ -20,11 +20,12 @@ cudaError_t launch_group(const uint16_t *V, int BH, int N, int k, int iters, int
                          int32_t *counts, float *centroids, void *ws, int32_t *dev_status, uint64_t limit_ns,
                          cudaStream_t st);
 
-struct PrepWorkspace {
-    size_t off_amax, off_inv, bytes;
-};
-PrepWorkspace prep_workspace_layout(int BH, int N);
 constexpr uint32_t kPrepQkHadamard = 1u;   // VCA_PREP_QK_HADAMARD
+constexpr uint32_t kPrepKSmooth = 2u;      // VCA_PREP_K_SMOOTH
+struct PrepWorkspace {
+    size_t off_amax, off_inv, off_ksum, off_kmean, bytes;
+};
+PrepWorkspace prep_workspace_layout(int BH, int N, uint32_t flags);
 cudaError_t launch_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int BH, int N,
                         int vmode, uint32_t flags, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res,
                         uint8_t *v_sf, float *v_scale, uint16_t *v_mean, void *ws, cudaStream_t st);

@@ -15,6 +15,11 @@
 //               run close together), subtract the stored mean, quantise, and
 //               write the residual channel-major (tokens contiguous per channel,
 //               the K-major operand layout of the PV contraction).
+// With K smoothing (SageAttention's treatment of the keys' channel bias: the
+// channel mean of K over the sequence is subtracted, which moves every score
+// of a query row by the same amount) the K quantisation moves to prep_vquant:
+// prep_stats writes each permuted block's channel sums, prep_scale adds them
+// in block order into the mean, prep_vquant quantises K - mean.
 #include "vca_device.cuh"
 #include "vca_internal.h"
 
@@ -39,24 +44,35 @@ __device__ __forceinline__ float block_max(float v, float *red) {
 }
 
 // Quantise one 128 x 128 bf16 block (rows given by `rows`, or contiguous from
-// `row0` when rows == nullptr) to E4M3 with the block's absmax scale.
+// `row0` when rows == nullptr) to E4M3 with the block's absmax scale.  With
+// kShift every value first has its channel's shift[c] subtracted (one fp32
+// rounding): the K smoothing.
+template <bool kShift>
+__device__ __forceinline__ float qk_value(uint32_t w, int half, int c, const float *shift) {
+    const float x = __uint_as_float(half ? (w & 0xFFFF0000u) : (w << 16));
+    if constexpr (kShift) return __fsub_rn(x, shift[c]);
+    return x;
+}
+
+template <bool kShift>
 __device__ __forceinline__ void quant_qk_block(const uint16_t *__restrict__ X, int64_t head_row0,
-                                               const int32_t *__restrict__ rows, int row0, uint8_t *__restrict__ out,
-                                               float *__restrict__ scale, float *red) {
+                                               const int32_t *__restrict__ rows, int row0, const float *shift,
+                                               uint8_t *__restrict__ out, float *__restrict__ scale, float *red) {
     const int tid = threadIdx.x;
     uint4 v[8];
     float amax = 0.0f;
+    const int c8 = (tid & 15) * 8;   // this thread's 8 channels (the same for every i)
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int u = i * kThreads + tid;
-        const int r = u >> 4, c8 = (u & 15) * 8;
+        const int r = u >> 4;
         const int64_t src = head_row0 + (rows ? rows[r] : row0 + r);
         v[i] = *reinterpret_cast<const uint4 *>(X + src * kD + c8);
         const uint32_t *w = reinterpret_cast<const uint32_t *>(&v[i]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            amax = fmaxf(amax, fabsf(__uint_as_float(w[j] << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xFFFF0000u)));
+            amax = fmaxf(amax, fabsf(qk_value<kShift>(w[j], 0, c8 + 2 * j, shift)));
+            amax = fmaxf(amax, fabsf(qk_value<kShift>(w[j], 1, c8 + 2 * j + 1, shift)));
         }
     }
     amax = block_max(amax, red);
@@ -73,10 +89,11 @@ __device__ __forceinline__ void quant_qk_block(const uint16_t *__restrict__ X, i
         uint32_t packed[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            packed[j] = e4m3x4(__fmul_rn(__uint_as_float(w[2 * j] << 16), inv),
-                               __fmul_rn(__uint_as_float(w[2 * j] & 0xFFFF0000u), inv),
-                               __fmul_rn(__uint_as_float(w[2 * j + 1] << 16), inv),
-                               __fmul_rn(__uint_as_float(w[2 * j + 1] & 0xFFFF0000u), inv));
+            const int c = c8 + 4 * j;
+            packed[j] = e4m3x4(__fmul_rn(qk_value<kShift>(w[2 * j], 0, c, shift), inv),
+                               __fmul_rn(qk_value<kShift>(w[2 * j], 1, c + 1, shift), inv),
+                               __fmul_rn(qk_value<kShift>(w[2 * j + 1], 0, c + 2, shift), inv),
+                               __fmul_rn(qk_value<kShift>(w[2 * j + 1], 1, c + 3, shift), inv));
         }
         *reinterpret_cast<uint2 *>(out + static_cast<int64_t>(u) * 8) = make_uint2(packed[0], packed[1]);
     }
@@ -89,11 +106,13 @@ __device__ __forceinline__ void quant_qk_block(const uint16_t *__restrict__ X, i
 // consecutive lanes, 8 per lane: bits 0-2 are butterflied in registers, bits
 // 3-6 (the lane's bits 0-3) across lanes.  The stored scale is amax / 448
 // times `post` (a power of two: 1 for Q, 1/128 for K, so that sq sk q8 . k8
-// still approximates q . k).
+// still approximates q . k).  With kShift the channel shift (K smoothing) is
+// subtracted before the rotation.
+template <bool kShift>
 __device__ __forceinline__ void quant_qk_block_hadamard(const uint16_t *__restrict__ X, int64_t head_row0,
                                                         const int32_t *__restrict__ rows, int row0, float post,
-                                                        uint8_t *__restrict__ out, float *__restrict__ scale,
-                                                        float *red) {
+                                                        const float *shift, uint8_t *__restrict__ out,
+                                                        float *__restrict__ scale, float *red) {
     const int tid = threadIdx.x, lane = tid & 31;
     float x[8][8];
     float amax = 0.0f;
@@ -106,8 +125,8 @@ __device__ __forceinline__ void quant_qk_block_hadamard(const uint16_t *__restri
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            x[i][2 * j] = __uint_as_float(w[j] << 16);
-            x[i][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+            x[i][2 * j] = qk_value<kShift>(w[j], 0, c8 + 2 * j, shift);
+            x[i][2 * j + 1] = qk_value<kShift>(w[j], 1, c8 + 2 * j + 1, shift);
         }
 #pragma unroll
         for (int h = 1; h < 8; h <<= 1)
@@ -148,6 +167,46 @@ __device__ __forceinline__ void quant_qk_block_hadamard(const uint16_t *__restri
     }
 }
 
+// K smoothing: the channel sums of one permuted 128-token K block in a fixed
+// fp32 order, a halving tree (token i plus token i + 64 for i < 64, then
+// i + 32, ..., i + 1).  Thread (t16 = tid / 16) holds tokens 16 i + t16 of
+// eight channels, so the first three levels stay in its registers
+// ((x_0 + x_4) + (x_2 + x_6)) + ((x_1 + x_5) + (x_3 + x_7)) over its i = 0..7;
+// the last four (over t16) run per channel from shared memory.
+__device__ __forceinline__ void k_block_tree_sums(const uint16_t *__restrict__ K, int64_t head_row0,
+                                                  const int32_t *__restrict__ rows, float *sPart,
+                                                  float *__restrict__ out) {
+    const int tid = threadIdx.x, t16 = tid >> 4, c8 = (tid & 15) * 8;
+    float x[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(K + (head_row0 + rows[16 * i + t16]) * kD + c8);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            x[i][2 * j] = __uint_as_float(w[j] << 16);
+            x[i][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+        }
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const float a0 = __fadd_rn(x[0][c], x[4][c]), a1 = __fadd_rn(x[1][c], x[5][c]);
+        const float a2 = __fadd_rn(x[2][c], x[6][c]), a3 = __fadd_rn(x[3][c], x[7][c]);
+        sPart[t16 * kD + c8 + c] = __fadd_rn(__fadd_rn(a0, a2), __fadd_rn(a1, a3));
+    }
+    __syncthreads();
+    if (tid < kD) {
+        float p[16];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) p[t] = sPart[t * kD + tid];
+#pragma unroll
+        for (int h = 8; h >= 1; h >>= 1)
+#pragma unroll
+            for (int t = 0; t < h; ++t) p[t] = __fadd_rn(p[t], p[t + h]);
+        out[tid] = p[0];
+    }
+}
+
 // Gather the block's 128 V rows into shared memory (token-major, padded rows)
 // as asynchronous 16-byte copies (cp.async): all of a thread's copies are in
 // flight at once, and the gather can run while the thread works on something
@@ -171,7 +230,7 @@ __device__ __forceinline__ void two_sum(float a, float b, float &s, float &e) {
     e = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
 }
 
-template <bool kHadamard>
+template <bool kHadamard, bool kSmooth>
 __global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__restrict__ Q,
                                                               const uint16_t *__restrict__ K,
                                                               const uint16_t *__restrict__ V,
@@ -179,7 +238,8 @@ __global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__
                                                               uint8_t *__restrict__ q8, float *__restrict__ sq,
                                                               uint8_t *__restrict__ k8, float *__restrict__ sk,
                                                               uint16_t *__restrict__ v_mean,
-                                                              float *__restrict__ amax_part) {
+                                                              float *__restrict__ amax_part,
+                                                              float *__restrict__ ksum) {
     // the V tile, then 2 x 2 x 128 floats of per-half partial results
     __shared__ __align__(16) uint16_t sV[kBlk * kRowStride + 4 * kD * 2];
     __shared__ float red[kThreads / 32];
@@ -188,16 +248,24 @@ __global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__
     const int32_t *rows = perm + head_row0 + static_cast<int64_t>(b) * kBlk;
     const int64_t blk_off = (head_row0 + static_cast<int64_t>(b) * kBlk) * kD;
 
-    // V's gather runs in the background while Q and K are quantised
+    // V's gather runs in the background while Q and K are quantised (K, with
+    // smoothing, waits for the sequence's mean: here only its block sums)
     load_v_tile_async(V, head_row0, rows, sV);
-    if constexpr (kHadamard) {
-        quant_qk_block_hadamard(Q, head_row0, nullptr, b * kBlk, 1.0f, q8 + blk_off,
-                                sq + static_cast<int64_t>(bh) * nb + b, red);
-        quant_qk_block_hadamard(K, head_row0, rows, 0, 1.0f / kD, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b,
-                                red);
+    if constexpr (kHadamard)
+        quant_qk_block_hadamard<false>(Q, head_row0, nullptr, b * kBlk, 1.0f, nullptr, q8 + blk_off,
+                                       sq + static_cast<int64_t>(bh) * nb + b, red);
+    else
+        quant_qk_block<false>(Q, head_row0, nullptr, b * kBlk, nullptr, q8 + blk_off,
+                              sq + static_cast<int64_t>(bh) * nb + b, red);
+    if constexpr (kSmooth) {
+        __shared__ float sPart[16 * kD];
+        k_block_tree_sums(K, head_row0, rows, sPart, ksum + (static_cast<int64_t>(bh) * nb + b) * kD);
+    } else if constexpr (kHadamard) {
+        quant_qk_block_hadamard<false>(K, head_row0, rows, 0, 1.0f / kD, nullptr, k8 + blk_off,
+                                       sk + static_cast<int64_t>(bh) * nb + b, red);
     } else {
-        quant_qk_block(Q, head_row0, nullptr, b * kBlk, q8 + blk_off, sq + static_cast<int64_t>(bh) * nb + b, red);
-        quant_qk_block(K, head_row0, rows, 0, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b, red);
+        quant_qk_block<false>(K, head_row0, rows, 0, nullptr, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b,
+                              red);
     }
     cp_async_wait_all();
     __syncthreads();
@@ -260,10 +328,19 @@ __global__ void __launch_bounds__(kThreads) prep_stats_kernel(const uint16_t *__
 
 // E4M3: per channel a_c -> v_scale = a_c / 448, inv_c = 448 / a_c.
 // NVFP4: g = max_c a_c / (6 * 448) -> v_scale[bh]; inv[bh][0] = 6 g, inv[bh][1] = g.
+// K smoothing (ksum != nullptr): the channel mean of K = the block sums added
+// in block order, divided by N (fp32).
 __global__ void __launch_bounds__(kD) prep_scale_kernel(int nb, int vmode, const float *__restrict__ amax_part,
-                                                        float *__restrict__ v_scale, float *__restrict__ inv) {
+                                                        float *__restrict__ v_scale, float *__restrict__ inv,
+                                                        const float *__restrict__ ksum, float *__restrict__ kmean,
+                                                        int N) {
     __shared__ float red[kD / 32];
     const int bh = blockIdx.x, ch = threadIdx.x;
+    if (ksum) {
+        float total = 0.0f;
+        for (int b = 0; b < nb; ++b) total = __fadd_rn(total, ksum[(static_cast<int64_t>(bh) * nb + b) * kD + ch]);
+        kmean[static_cast<int64_t>(bh) * kD + ch] = __fdiv_rn(total, static_cast<float>(N));
+    }
     float a = 0.0f;
     for (int b = 0; b < nb; ++b) a = fmaxf(a, amax_part[(static_cast<int64_t>(bh) * nb + b) * kD + ch]);
     if (vmode == 0) {
@@ -286,17 +363,36 @@ __global__ void __launch_bounds__(kD) prep_scale_kernel(int nb, int vmode, const
     }
 }
 
+template <bool kSmooth, bool kHadamard>
 __global__ void __launch_bounds__(kThreads) prep_vquant_kernel(const uint16_t *__restrict__ V,
                                                                const int32_t *__restrict__ perm, int N, int vmode,
                                                                const uint16_t *__restrict__ v_mean,
                                                                const float *__restrict__ inv,
                                                                uint8_t *__restrict__ v_res,
-                                                               uint8_t *__restrict__ v_sf) {
+                                                               uint8_t *__restrict__ v_sf,
+                                                               const uint16_t *__restrict__ K,
+                                                               const float *__restrict__ kmean,
+                                                               uint8_t *__restrict__ k8, float *__restrict__ sk) {
     __shared__ __align__(16) uint16_t sV[kBlk * kRowStride];
     const int b = blockIdx.x, bh = blockIdx.y, nb = gridDim.x;
     const int64_t head_row0 = static_cast<int64_t>(bh) * N;
     const int32_t *rows = perm + head_row0 + static_cast<int64_t>(b) * kBlk;
     load_v_tile_async(V, head_row0, rows, sV);
+    if constexpr (kSmooth) {
+        // K smoothing: the permuted K block minus the channel mean, quantised
+        // while V's gather is in flight
+        __shared__ float sShift[kD];
+        __shared__ float red[kThreads / 32];
+        if (threadIdx.x < kD) sShift[threadIdx.x] = kmean[static_cast<int64_t>(bh) * kD + threadIdx.x];
+        __syncthreads();
+        const int64_t blk_off = (head_row0 + static_cast<int64_t>(b) * kBlk) * kD;
+        if constexpr (kHadamard)
+            quant_qk_block_hadamard<true>(K, head_row0, rows, 0, 1.0f / kD, sShift, k8 + blk_off,
+                                          sk + static_cast<int64_t>(bh) * nb + b, red);
+        else
+            quant_qk_block<true>(K, head_row0, rows, 0, sShift, k8 + blk_off, sk + static_cast<int64_t>(bh) * nb + b,
+                                 red);
+    }
     cp_async_wait_all();
     __syncthreads();
     const int ch = threadIdx.x & (kD - 1);
@@ -353,34 +449,57 @@ __global__ void __launch_bounds__(kThreads) prep_vquant_kernel(const uint16_t *_
 
 }  // namespace
 
-PrepWorkspace prep_workspace_layout(int BH, int N) {
+PrepWorkspace prep_workspace_layout(int BH, int N, uint32_t flags) {
     PrepWorkspace w;
     const size_t nb = static_cast<size_t>(N) / kBlk;
+    const size_t per_block = (sizeof(float) * BH * nb * kD + 255) & ~size_t(255);
+    const size_t per_head = (sizeof(float) * BH * kD + 255) & ~size_t(255);
     w.off_amax = 0;
-    const size_t amax_bytes = (sizeof(float) * BH * nb * kD + 255) & ~size_t(255);
-    w.off_inv = amax_bytes;
-    w.bytes = amax_bytes + ((sizeof(float) * BH * kD + 255) & ~size_t(255));
+    w.off_inv = per_block;
+    w.bytes = per_block + per_head;
+    w.off_ksum = w.off_kmean = 0;
+    if (flags & kPrepKSmooth) {   // the K block sums and the K mean
+        w.off_ksum = w.bytes;
+        w.off_kmean = w.off_ksum + per_block;
+        w.bytes = w.off_kmean + per_head;
+    }
     return w;
 }
 
 cudaError_t launch_prep(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm, int BH, int N,
                         int vmode, uint32_t flags, uint8_t *q8, float *sq, uint8_t *k8, float *sk, uint8_t *v_res,
                         uint8_t *v_sf, float *v_scale, uint16_t *v_mean, void *ws, cudaStream_t st) {
-    const PrepWorkspace w = prep_workspace_layout(BH, N);
+    const PrepWorkspace w = prep_workspace_layout(BH, N, flags);
     unsigned char *base = static_cast<unsigned char *>(ws);
     float *amax = reinterpret_cast<float *>(base + w.off_amax);
     float *inv = reinterpret_cast<float *>(base + w.off_inv);
+    const bool smooth = (flags & kPrepKSmooth) != 0, had = (flags & kPrepQkHadamard) != 0;
+    float *ksum = smooth ? reinterpret_cast<float *>(base + w.off_ksum) : nullptr;
+    float *kmean = smooth ? reinterpret_cast<float *>(base + w.off_kmean) : nullptr;
     const int nb = N / kBlk;
-    if (flags & kPrepQkHadamard)
-        prep_stats_kernel<true><<<dim3(nb, BH), kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax);
+    const dim3 grid(nb, BH);
+    if (had && smooth)
+        prep_stats_kernel<true, true><<<grid, kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax, ksum);
+    else if (had)
+        prep_stats_kernel<true, false><<<grid, kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax, ksum);
+    else if (smooth)
+        prep_stats_kernel<false, true><<<grid, kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax, ksum);
     else
-        prep_stats_kernel<false><<<dim3(nb, BH), kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax);
+        prep_stats_kernel<false, false><<<grid, kThreads, 0, st>>>(Q, K, V, perm, N, q8, sq, k8, sk, v_mean, amax, ksum);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    prep_scale_kernel<<<BH, kD, 0, st>>>(nb, vmode, amax, v_scale, inv);
+    prep_scale_kernel<<<BH, kD, 0, st>>>(nb, vmode, amax, v_scale, inv, ksum, kmean, N);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    prep_vquant_kernel<<<dim3(nb, BH), kThreads, 0, st>>>(V, perm, N, vmode, v_mean, inv, v_res, v_sf);
+    if (smooth && had)
+        prep_vquant_kernel<true, true><<<grid, kThreads, 0, st>>>(V, perm, N, vmode, v_mean, inv, v_res, v_sf, K, kmean,
+                                                                  k8, sk);
+    else if (smooth)
+        prep_vquant_kernel<true, false><<<grid, kThreads, 0, st>>>(V, perm, N, vmode, v_mean, inv, v_res, v_sf, K,
+                                                                   kmean, k8, sk);
+    else
+        prep_vquant_kernel<false, false><<<grid, kThreads, 0, st>>>(V, perm, N, vmode, v_mean, inv, v_res, v_sf, K,
+                                                                    kmean, k8, sk);
     return cudaGetLastError();
 }
 

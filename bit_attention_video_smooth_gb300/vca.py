@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libvca.so")
 
 VCA_OK, VCA_ERR_INVALID_ARG, VCA_ERR_UNSUPPORTED, VCA_ERR_CUDA, VCA_ERR_TIMEOUT, VCA_ERR_WORKSPACE = range(6)
 VCA_V_E4M3, VCA_V_NVFP4 = 0, 1
-VCA_OP_GROUP, VCA_OP_PREP, VCA_OP_ATTENTION = 0, 1, 2
+VCA_OP_GROUP, VCA_OP_PREP, VCA_OP_ATTENTION, VCA_OP_PREP_KSMOOTH = 0, 1, 2, 3
 
 # Entry points declared in include/vca.h (the ABI test checks they are exported).
 EXPORTS = ("vca_status_string", "vca_version", "vca_workspace_bytes", "vca_group", "vca_prep_quant",
@@ -153,6 +153,7 @@ def vca_prep_quant(Q, K, V, perm, vmode: int, q8, sq, k8, sk, v_res, v_sf, v_sca
 
 
 VCA_PREP_QK_HADAMARD = 1
+VCA_PREP_K_SMOOTH = 2
 
 
 def _prep_buffers(where, B, H, N, d, vmode, Q, K, V, perm, q8, sq, k8, sk, v_res, v_sf, v_scale, v_mean,
@@ -265,9 +266,10 @@ def alloc_group(B, H, N, k, device="cuda") -> Grouped:
                    torch.empty((BH, k, 128), dtype=torch.float32, device=device), ws)
 
 
-def alloc_prep(B, H, N, vmode=VCA_V_E4M3, device="cuda") -> Prepared:
+def alloc_prep(B, H, N, vmode=VCA_V_E4M3, device="cuda", k_smooth: bool = False) -> Prepared:
     BH, nb, d = B * H, N // 128, 128
-    ws = torch.empty(max(16, vca_workspace_bytes(VCA_OP_PREP, B, H, N, d, 1, vmode)), dtype=torch.uint8, device=device)
+    op = VCA_OP_PREP_KSMOOTH if k_smooth else VCA_OP_PREP
+    ws = torch.empty(max(16, vca_workspace_bytes(op, B, H, N, d, 1, vmode)), dtype=torch.uint8, device=device)
     if vmode == VCA_V_E4M3:
         v_res = torch.empty((BH, nb, d, 128), dtype=torch.uint8, device=device)
         v_sf = None
@@ -293,10 +295,10 @@ def group(V: torch.Tensor, k: int, iters: int, out: Optional[Grouped] = None,
 
 
 def prep_quant(Q, K, V, perm, vmode=VCA_V_E4M3, out: Optional[Prepared] = None,
-               qk_hadamard: bool = False) -> Prepared:
+               qk_hadamard: bool = False, k_smooth: bool = False) -> Prepared:
     B, H, N, _ = Q.shape
-    p = out or alloc_prep(B, H, N, vmode, Q.device)
-    flags = VCA_PREP_QK_HADAMARD if qk_hadamard else 0
+    p = out or alloc_prep(B, H, N, vmode, Q.device, k_smooth=k_smooth)
+    flags = (VCA_PREP_QK_HADAMARD if qk_hadamard else 0) | (VCA_PREP_K_SMOOTH if k_smooth else 0)
     vca_prep_quant_ex(Q, K, V, perm, vmode, flags, p.q8, p.sq, p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean,
                       p.ws)
     return p

@@ -64,7 +64,8 @@ typedef enum {
 } vca_status;
 
 typedef enum { VCA_V_E4M3 = 0, VCA_V_NVFP4 = 1 } vca_vmode;
-typedef enum { VCA_OP_GROUP = 0, VCA_OP_PREP = 1, VCA_OP_ATTENTION = 2 } vca_op;
+/* VCA_OP_PREP_KSMOOTH: the prep's workspace when VCA_PREP_K_SMOOTH is set. */
+typedef enum { VCA_OP_GROUP = 0, VCA_OP_PREP = 1, VCA_OP_ATTENTION = 2, VCA_OP_PREP_KSMOOTH = 3 } vca_op;
 
 /* Human-readable name of a vca_status value (static string, never NULL). */
 const char *vca_status_string(int status);
@@ -134,8 +135,22 @@ int vca_prep_quant(const uint16_t *Q, const uint16_t *K, const uint16_t *V, cons
  *          the channel index, every pair (c, c + 2^k) with bit k of c clear
  *          becomes (a + b, a - b) -- so its rounding is reproducible; then
  *          s = amax / 448 and x8 = E4M3_rne_sat(x * (448 / amax)) as usual.
+ *   VCA_PREP_K_SMOOTH  subtract the keys' channel mean over the sequence of
+ *          each (b,h) before the FP8 quantisation (SageAttention's treatment
+ *          of the keys' channel bias, the handling of Q/K outliers the paper
+ *          page's motivation and the insight page's section "Value Is the
+ *          Error Source Earlier Methods Underestimated" refer to).  Every score
+ *          of a query row moves by the same amount, so softmax attention is
+ *          unchanged and vca_attention needs no change.  The mean is fp32 in a
+ *          fixed order, so it is reproducible: per permuted 128-token block a
+ *          halving tree (token i plus token i + 64 for i < 64, then i + 32, ...,
+ *          i + 1), the block sums added in block order, divided by N; each key
+ *          value becomes fp32(k) - mean (one rounding), before the Hadamard
+ *          rotation when both flags are set.  Needs ws_bytes >=
+ *          vca_workspace_bytes(VCA_OP_PREP_KSMOOTH, ...).
  */
 #define VCA_PREP_QK_HADAMARD 1u
+#define VCA_PREP_K_SMOOTH 2u
 int vca_prep_quant_ex(const uint16_t *Q, const uint16_t *K, const uint16_t *V, const int32_t *perm,
                       int B, int H, int N, int d, int vmode, uint32_t flags,
                       uint8_t *q8, float *sq, uint8_t *k8, float *sk,

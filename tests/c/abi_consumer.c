@@ -38,7 +38,7 @@ int main(void) {
     check(vca_group(fake16, 1, 2, 1024, 128, 8, 4, fake32, fake32, NULL, NULL, NULL, 0, NULL, NULL)
               == VCA_ERR_WORKSPACE,
           "group without a workspace");
-    check(vca_prep_quant_ex(fake16, fake16, fake16, fake32, 1, 2, 1024, 128, VCA_V_E4M3, 2u, fake8, fakef, fake8,
+    check(vca_prep_quant_ex(fake16, fake16, fake16, fake32, 1, 2, 1024, 128, VCA_V_E4M3, 4u, fake8, fakef, fake8,
                             fakef, fake8, NULL, fakef, fake16, fake8, 1u << 30, NULL) == VCA_ERR_INVALID_ARG,
           "prep with an undefined flag");
     return failures;

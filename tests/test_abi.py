@@ -58,6 +58,8 @@ def test_workspace_sizes(lib):
     assert ws(0, 1, 16, 1 << 27, 128, 8, 0) == 0    # B*H*N = 2^31 tokens
     assert ws(0, 0, 2, 1024, 128, 8, 0) == 0        # empty batch
     assert ws(1, 1, 2, 0, 128, 8, 0) == 0           # empty sequence
+    # K smoothing adds the block sums (512 B a block) and the mean (512 B a head)
+    assert ws(3, 1, 2, 1024, 128, 1, 0) == ws(1, 1, 2, 1024, 128, 1, 0) + 2 * 8 * 512 + 2 * 512
 
 
 def test_invalid_arguments_rejected_without_cuda(lib):
@@ -75,6 +77,12 @@ def test_invalid_arguments_rejected_without_cuda(lib):
     assert lib.vca_attention(*([fake] * 8), 1, 2, 0, 128, 0.0, 1, 0, fake, None, None) == 1
     # ExpCast has no NVFP4 counterpart
     assert lib.vca_attention(*([fake] * 8), 1, 2, 1024, 128, 0.0, 1, 1, fake, None, None) == 2
+    # K smoothing wants its larger workspace: the plain prep's size is rejected before any launch
+    lib.vca_workspace_bytes.restype = ctypes.c_size_t
+    lib.vca_prep_quant_ex.argtypes = [P] * 4 + [ctypes.c_int] * 5 + [ctypes.c_uint32] + [P] * 9 + \
+        [ctypes.c_size_t, P]
+    plain_ws = lib.vca_workspace_bytes(1, 1, 2, 1024, 128, 1, 0)
+    assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1024, 128, 0, 2, *([fake] * 9), plain_ws, None) == 5
     lib.vca_group.argtypes = [P, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                               ctypes.c_int, P, P, P, P, P, ctypes.c_size_t, P, P]
     assert lib.vca_group(fake, 1, 2, 1024, 128, 8, 0, fake, fake, None, None, fake, 1 << 30, None, None) == 1  # iters
@@ -85,10 +93,10 @@ def test_invalid_arguments_rejected_without_cuda(lib):
                          None) == 1                                                                       # status
     lib.vca_selftest_timeout.argtypes = [P, ctypes.c_uint64, P]
     assert lib.vca_selftest_timeout(fake, 10, None) == 1
-    # prep option flags: only VCA_PREP_QK_HADAMARD (bit 0) is defined
+    # prep option flags: VCA_PREP_QK_HADAMARD (bit 0) and VCA_PREP_K_SMOOTH (bit 1) are defined
     lib.vca_prep_quant_ex.argtypes = [P, P, P, P] + [ctypes.c_int] * 5 + [ctypes.c_uint32] + [P] * 8 + \
         [P, ctypes.c_size_t, P]
-    assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1024, 128, 0, 2, *([fake] * 8), fake, 1 << 30, None) == 1
+    assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1024, 128, 0, 4, *([fake] * 8), fake, 1 << 30, None) == 1
     assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1000, 128, 0, 1, *([fake] * 8), fake, 1 << 30, None) == 1
     assert lib.vca_prep_quant_ex(*([fake] * 4), 1, 2, 1024, 128, 0, 1, *([fake] * 8), None, 0, None) == 5
 

@@ -89,6 +89,26 @@ def test_fullsize_qk_hadamard_prep(V, orc):
         assert np.array_equal(p.sk[h].cpu().numpy(), ref["sk"][0])
 
 
+def test_fullsize_k_smooth_prep(V, orc):
+    """The K smoothing prep option at the Wan shape, all heads in one launch:
+    the smoothed and quantised K (and Q) of sampled heads match the oracle bit
+    for bit -- the channel mean is summed over 552 blocks in the documented
+    order."""
+    w = I.WORKLOADS["wan"]
+    Q, K, Vv = I.make_qkv(w, seed=63, device="cuda")
+    perm = I.random_perm(w.BH, w.N, seed=64, device="cuda")
+    p = V.prep_quant(Q, K, Vv, perm, V.VCA_V_E4M3, k_smooth=True)
+    torch.cuda.synchronize()
+    Qf, Kf, Vf = (t.view(w.BH, w.N, 128) for t in (Q, K, Vv))
+    for h in (3, w.BH - 2):
+        ref = orc.prep(_u16(Qf[h])[None], _u16(Kf[h])[None], _u16(Vf[h])[None], perm[h].cpu().numpy()[None],
+                       k_smooth=True)
+        assert np.array_equal(p.q8[h].cpu().numpy(), ref["q8"][0])
+        assert np.array_equal(p.k8[h].cpu().numpy(), ref["k8"][0])
+        assert np.array_equal(p.sq[h].cpu().numpy(), ref["sq"][0])
+        assert np.array_equal(p.sk[h].cpu().numpy(), ref["sk"][0])
+
+
 def test_fullsize_group_sampled_heads(V, orc):
     """k-means at the Wan shape on sampled heads.
 

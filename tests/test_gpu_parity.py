@@ -211,6 +211,53 @@ def test_prep_qk_hadamard_parity(V, orc, BH, N, seed):
     assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
 
 
+@pytest.mark.parametrize("BH,N,seed,hadamard", [(2, 1024, 20, False), (3, 384, 21, False), (1, 2432, 22, False),
+                                                 (2, 640, 23, True)])
+def test_prep_k_smooth_parity(V, orc, BH, N, seed, hadamard):
+    """The K smoothing option: the device's block tree sums, their sum in block
+    order and the division by N give the oracle's channel mean bit for bit, so
+    q8, k8, sq and sk match exactly (with and without the QK Hadamard); the V
+    outputs are those of the plain prep; attention over the smoothed operands
+    matches the oracle's.  The keys carry a channel bias, the case smoothing
+    is for."""
+    q, k, v, perm = _prep_inputs(BH, N, seed)
+    k = k.float()
+    k[..., :6] += 5.0
+    k = k.to(torch.bfloat16)
+    q16, k16, v16 = (I.to_u16(t).reshape(BH, N, 128) for t in (q, k, v))
+    ref = orc.prep(q16, k16, v16, perm.numpy(), qk_hadamard=hadamard, k_smooth=True)
+    p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_E4M3, qk_hadamard=hadamard, k_smooth=True)
+    torch.cuda.synchronize()
+    assert np.array_equal(p.q8.cpu().numpy(), ref["q8"])
+    assert np.array_equal(p.k8.cpu().numpy(), ref["k8"])
+    assert np.array_equal(p.sq.cpu().numpy(), ref["sq"])
+    assert np.array_equal(p.sk.cpu().numpy(), ref["sk"])
+    plain = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_E4M3, qk_hadamard=hadamard)
+    torch.cuda.synchronize()
+    assert torch.equal(plain.v_res, p.v_res) and torch.equal(plain.v_mean.view(torch.int16), p.v_mean.view(torch.int16))
+    assert torch.equal(plain.q8, p.q8)
+    O = V.attention(p, 1, BH, N, expcast=True)
+    torch.cuda.synchronize()
+    O_ref = orc.attention(ref, orc.P_EXPCAST)
+    rel, mx = _o_close(O.view(torch.int16).cpu().numpy().view(np.uint16).reshape(BH, N, 128), O_ref)
+    assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
+
+
+def test_prep_k_smooth_needs_its_workspace(V):
+    """The smoothing prep asks for more workspace (the block sums and the mean):
+    a workspace sized for the plain prep is rejected before any launch."""
+    B, H, N = 1, 2, 512
+    plain = V.vca_workspace_bytes(V.VCA_OP_PREP, B, H, N)
+    smooth = V.vca_workspace_bytes(V.VCA_OP_PREP_KSMOOTH, B, H, N)
+    assert smooth > plain
+    q, k, v, perm = _prep_inputs(B * H, N, 30)
+    p = V.alloc_prep(B, H, N, V.VCA_V_E4M3)
+    with pytest.raises(V.VCAError) as e:
+        V.vca_prep_quant_ex(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_E4M3, V.VCA_PREP_K_SMOOTH, p.q8, p.sq,
+                            p.k8, p.sk, p.v_res, p.v_sf, p.v_scale, p.v_mean, p.ws)
+    assert e.value.status == V.VCA_ERR_WORKSPACE
+
+
 def test_prep_nvfp4_parity(V, orc):
     BH, N = 2, 1024
     q, k, v, perm = _prep_inputs(BH, N, 4)
