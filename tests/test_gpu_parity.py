@@ -265,6 +265,11 @@ def test_prep_nvfp4_parity(V, orc):
     p = V.prep_quant(q.cuda(), k.cuda(), v.cuda(), perm.cuda(), V.VCA_V_NVFP4)
     torch.cuda.synchronize()
     assert np.array_equal(p.q8.cpu().numpy(), ref["q8"])
+    assert np.array_equal(p.k8.cpu().numpy(), ref["k8"])
+    assert np.array_equal(p.sq.cpu().numpy(), ref["sq"])
+    assert np.array_equal(p.sk.cpu().numpy(), ref["sk"])
+    vm = p.v_mean.view(torch.int16).cpu().numpy().view(np.uint16)
+    assert (vm == ref["v_mean"]).mean() >= 0.9999
     np.testing.assert_allclose(p.v_scale.cpu().numpy(), ref["v_scale"], rtol=1e-6)
     assert (p.v_sf.cpu().numpy() == ref["v_sf"]).mean() >= 0.9999
     assert (p.v_res.cpu().numpy() == ref["v_res"]).mean() >= 0.9999
