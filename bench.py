@@ -198,8 +198,10 @@ def oracle_sample(w, seed: int = 0):
 
     oracle.build()
     cores = oracle.threads()
-    heads = max(1, min(w.BH, cores))
-    rows_per_head = 64
+    # 1024 query rows per head (always the first and last blocks' edge rows) on
+    # two heads: about 10 s of oracle work on 16 cores at the Wan shape
+    heads = max(1, min(w.BH, 2))
+    rows_per_head = 1024
     sub = I.with_n(w, w.N, H=heads, B=1)
     q, k, v = (I.to_u16(t).reshape(heads, w.N, 128) for t in I.make_qkv(sub, seed=seed))
     rows = I.sample_rows(w.N, rows_per_head, seed=seed).numpy()
@@ -254,6 +256,13 @@ def dist_barrier(ws: int):
 
 
 # ---------------------------------------------------------------------------
+def workload_config(w, n_gpus):
+    """The `config` of a bench line (both arms print the same one)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k, "iters": w.iters,
+            "vmode": w.vmode, "expcast": w.expcast, "parallelism": f"replicas x{n_gpus}",
+            "l2": f"inputs (3 x {w.BH * w.N * 256 / 1e6:.0f} MB) exceed L2; no flush"}
+
+
 def run_reference(args, w, ws, rank):
     if rank != 0:
         return
@@ -270,8 +279,7 @@ def run_reference(args, w, ws, rank):
         "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64/f32 (oracle)", "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k, "iters": w.iters,
-                   "vmode": w.vmode, "expcast": w.expcast},
+        "config": workload_config(w, args.gpus),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -404,9 +412,7 @@ def run_ours(args, w, ws, rank, local):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if vmode == 0 else "e4m3/e2m1",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "d": w.d, "k": w.k, "iters": w.iters,
-                   "vmode": w.vmode, "expcast": w.expcast, "parallelism": f"replicas x{ws}",
-                   "l2": f"inputs (3 x {w.BH * w.N * 256 / 1e6:.0f} MB) exceed L2; no flush"},
+        "config": workload_config(w, ws),
         "breakdown_ms": {"group": t_group, "prep": t_prep, "attention": t_attn},
         "attention_tflops": achieved,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
