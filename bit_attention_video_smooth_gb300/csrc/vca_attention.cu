@@ -78,7 +78,9 @@ constexpr uint32_t kVStageBytes = kOnesBytes + kTileBytes + kOnesBytes;   // [on
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kOffMA = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
-constexpr uint32_t kOffRS = kOffMB + kTileBytes;             // fp32 [kRsSlots][128] row sums (block j in slot j % 32)
+constexpr uint32_t kMeanGroupBytes = kMeanJ * kD * 2;        // bf16 means of 16 key blocks
+constexpr uint32_t kOffMean = kOffMB + kTileBytes;           // bf16 [2][16][128]: group g in buffer g & 1
+constexpr uint32_t kOffRS = kOffMean + 2 * kMeanGroupBytes;  // fp32 [kRsSlots][128] row sums (block j in slot j % 32)
 constexpr uint32_t kOffRSM = kOffRS + kRsSlots * kBlk * 4;   // fp32 [kRsSlots][128] the max each sum is taken against
 constexpr uint32_t kOffSV = kOffRSM + kRsSlots * kBlk * 4;   // fp32 [128] residual scales
 constexpr uint32_t kOffMX = kOffSV + kBlk * 4;               // fp32 [2][128] reference max handed over, per parity
@@ -176,7 +178,7 @@ __device__ __forceinline__ void codes32(const uint32_t (&X)[kCols], float c, flo
 // `row`): A row = the row sums from their ring slots, each brought from the
 // reference max it was taken against to m; B row = mean / s_v.
 __device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
-                                            const uint16_t *vmh, const float *sSV, unsigned char *sMA,
+                                            const uint16_t *sMeanGroup, const float *sSV, unsigned char *sMA,
                                             unsigned char *sMB) {
     float hi[kMeanJ], lo[kMeanJ];
 #pragma unroll
@@ -191,7 +193,7 @@ __device__ __forceinline__ void stage_means(int row, const float *sRS, const flo
     const float inv_sv = 1.0f / sSV[row];
 #pragma unroll
     for (int i = 0; i < kMeanJ; ++i)
-        split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
+        split_bf16(__fmul_rn(bf16_bits_to_f32(sMeanGroup[i * kD + row]), inv_sv), hi[i], lo[i]);
     store_mean_row(sMB, row, hi, lo, false);
 }
 
@@ -288,8 +290,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; b < nb; ++b) {
                 const int s = b % stages, use = b / stages;
                 if (use > 0 && !mbar_wait(empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) break;
-                mbar_expect_tx(full + s, kTileBytes);
+                // with V(16 g) the bf16 means of group g (blocks 16 g .. 16 g + 15), on
+                // the same barrier, into buffer g & 1: PV(16 g) complete implies they
+                // have landed.  The group that buffer held (g - 2) was staged at block
+                // 16 g - 13, before PV(16 g - 3) completed, which this refill waited for.
+                const bool with_means = !is_k && (b % kMeanJ) == 0;
+                const uint32_t mean_bytes =
+                    with_means ? static_cast<uint32_t>(nb - b < kMeanJ ? nb - b : kMeanJ) * kD * 2 : 0u;
+                mbar_expect_tx(full + s, kTileBytes + mean_bytes);
                 tma_load_2d(ring + s * stride, tm, full + s, 0, is_k ? bh * N + b * kBlk : (bh * nb + b) * kBlk);
+                if (with_means)
+                    bulk_load(smem + kOffMean + ((b / kMeanJ) & 1) * kMeanGroupBytes,
+                              p.v_mean + (static_cast<int64_t>(bh) * nb + b) * kD, mean_bytes, full + s);
                 armed[s] = use + 1;
             }
             // every copy this thread issued has landed before the CTA can exit
@@ -485,7 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (ok && flush_after(b)) {
                     // mean-restore operands of blocks b-19 .. b-4 (the MMA follows PV(b))
-                    stage_means(row, sRS, sRSM, m_new, b - kMeanJ - kMeanLag, vmh, sSV, sMA, sMB);
+                    // the group's means landed with V(b0), before PV(b0) could run
+                    const int b0 = b - kMeanJ - kMeanLag;
+                    stage_means(row, sRS, sRSM, m_new, b0,
+                                reinterpret_cast<const uint16_t *>(smem + kOffMean) + ((b0 / kMeanJ) & 1) * (kMeanJ * kD),
+                                sSV, sMA, sMB);
                     fence_proxy_async_smem();   // read by the tensor core
                 }
                 if (ok) {

@@ -73,10 +73,13 @@ def test_e4m3_shared_memory_layout(e4m3):
     assert c["kOffBar"] % 8 == 0
     assert c["kSmemBytes"] <= 232448
     # the regions follow one another without overlap
-    order = ["kOffK", "kOffV", "kOffMA", "kOffMB", "kOffRS", "kOffRSM", "kOffSV", "kOffMX", "kOffL", "kOffBar",
-             "kOffMisc"]
+    order = ["kOffK", "kOffV", "kOffMA", "kOffMB", "kOffMean", "kOffRS", "kOffRSM", "kOffSV", "kOffMX", "kOffL",
+             "kOffBar", "kOffMisc"]
     offs = [c[k] for k in order]
     assert offs == sorted(offs)
+    # the means of two 16-block groups: bulk-copy destinations (16-byte aligned)
+    assert c["kOffMean"] % 16 == 0 and c["kOffRS"] - c["kOffMean"] == 2 * c["kMeanGroupBytes"]
+    assert c["kMeanGroupBytes"] == c["kMeanJ"] * 128 * 2
     assert c["kOffRSM"] - c["kOffRS"] == c["kRsSlots"] * 128 * 4
     # one mbarrier each: q_full, K and V full/empty rings, s_full, s_free, p_full, pv_done, drain (two each)
     assert c["kNumBars"] == 1 + 2 * c["kKStages"] + 2 * c["kVStages"] + 2 * 5
