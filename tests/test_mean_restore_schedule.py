@@ -40,7 +40,8 @@ def K():
     assert "return b >= kMeanJ + kMeanLag && (b % kMeanJ) == kMeanLag;" in kern
     assert "const int bf = nb - 1 >= kMeanJ + kMeanLag ? kMeanLag + kMeanJ * ((nb - 1 - kMeanLag) / kMeanJ) : -1;" in kern
     assert "const int tail0 = bf >= 0 ? bf - kMeanLag : 0;" in kern
-    assert "stage_means(row, sRS, sRSM, m_new, b - kMeanJ - kMeanLag, vmh, sSV, sMA, sMB);" in kern
+    assert "const int b0 = b - kMeanJ - kMeanLag;" in kern
+    assert "stage_means(row, sRS, sRSM, m_new, b0," in kern
     return {"J": _const(common, "kMeanJ"), "L": _const(kern, "kMeanLag"), "S": _const(common, "kRsSlots"),
             "blk": 128, "d": 128, "tile_bytes": 128 * 128}
 
