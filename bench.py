@@ -156,9 +156,9 @@ def attention_traffic(w):
 # reported beside the measured one.
 NOMINAL_TFLOPS = {"bf16": 2250.0, "fp8": 4500.0, "fp4": 13500.0}
 # The rate each attention kernel's two contractions run at (QK, PV): the
-# E4M3 kernel runs both as FP8 MMAs; the NVFP4 kernel runs QK as FP8 and PV on
-# exactly decoded f16 operands.
-ATTN_RATES = {"e4m3": ("fp8", "fp8"), "nvfp4": ("fp8", "bf16")}
+# E4M3 kernel runs both as FP8 MMAs; the NVFP4 kernel runs QK as FP8 and PV as
+# the block-scaled FP4 MMA.
+ATTN_RATES = {"e4m3": ("fp8", "fp8"), "nvfp4": ("fp8", "fp4")}
 
 
 def _bound(rates, tflops):

@@ -5,31 +5,40 @@
 // scale per 16 keys of a row), with the V-Smooth mean restore of the 8-bit
 // kernel.
 //
-// PV runs on the tensor core as kind::f16 on the decoded operands: an E2M1
-// value times an E4M3 scale has at most 6 significant bits and lies in
-// [2^-10, 2688] (V) or [2^-10, 256] (P), so decoded P and decoded V are exact
-// in f16 and the MMA forms exactly the products a block-scaled FP4 MMA forms,
-// summed in fp32.  QK stays E4M3 (kind::f8f6f4).
+// PV runs on the tensor core as the block-scaled FP4 MMA (kind::mxf4nvf4,
+// scale_vec::4X): P (A, E2M1 codes from TMEM) times V (B, E2M1 codes from
+// shared memory), each 16 keys of a row of either operand scaled by its E4M3
+// scale factor, which the MMA reads from TMEM; fp32 accumulation.  QK stays
+// E4M3 (kind::f8f6f4).  Layouts (measured on the hardware with a probe): P key k
+// at TMEM column k / 8, nibble k % 8; row m's four scales of a 64-key MMA in
+// lane m, column sfa + m / 32; B row n's, for the D rows of lane quarter q,
+// in lane 32 q + n % 32, column sfb + n / 32, so the V scales (and the ones'
+// scales of the row-sum MMA) are present in all four lane quarters; the V
+// codes as a 128-byte-swizzled K-major tile whose 128-byte rows (one per
+// channel) carry the block's 128 keys in their first 64 bytes.
 //
 // One CTA owns a 128-row query tile of one (batch, head).  Warp roles:
-//   warp 0       TMA producer: K tiles into a 3-stage ring
+//   warp 11      TMA producer: K tiles into a 3-stage ring
 //   warp 1       TMEM owner and MMA issuer (one thread); per key block j:
-//                  [E | O] += P_j [ones ; Vhat_j]   (kind::f16, N = 144: the 16
-//                             extra columns are P_j's row sums), then the
-//                             mean-restore MMA when due, then
-//                  S[j&1] = Q8 K8_{j+2}^T             (kind::f8f6f4)
-//   warps 10-11  V decode: two channels per thread; E2M1 x E4M3 -> f16 in the
-//                128-byte-swizzled K-major layout of the PV B operand.  Lane 0
-//                of warp 10 also bulk-copies block j+3's packed codes (8 KB)
-//                and scales (1 KB) into a 4-stage ring.
+//                  O += P_j V_j, E_{j&1} = P_j ones  (two block-scaled MMAs
+//                                 each, K = 64; the second gives P_j's row sums)
+//                  then the mean-restore MMA when due, then
+//                  S[j&1] = Q8 K8_{j+2}^T               (kind::f8f6f4)
+//   warps 0, 10  V layout: each block's packed codes (8 KB) into the swizzled
+//                tile, two channels per thread, and its scale factors into
+//                the 32-row matrices the MMA issuer copies into TMEM (one
+//                copy fills all four lane quarters); warp 0's lane 0
+//                bulk-copies block j+3's codes and scales into a 4-stage ring.
 //   warps 2-9    softmax, two threads per query row (column halves): running
 //                max with the lazy threshold, NVFP4 P of the row against it,
-//                P into TMEM once PV(j-1) is done, row sum of block j-1 from
-//                its TMEM slot, O rescale, mean-restore operands, epilogue.
-// P has a single TMEM buffer (the budget holds no second one), so P_j is
-// written after PV(j-1) completes; the softmax computes P_j while PV(j-1) runs.
-// TMEM columns: S0 [0,128), S1 [128,256), E0 [256,272), O [272,400),
-// E1 [400,416), P [416,480) (f16, two keys per column), Q [480,512).
+//                P codes and scales into TMEM once PV(j-1) is done, row sum of
+//                block j-1 from its TMEM slot, O rescale, mean-restore
+//                operands, epilogue.
+// P has a single TMEM buffer, so P_j is written after PV(j-1) completes; the
+// softmax computes it while PV(j-1) runs.
+// TMEM columns: S0 [0,128), S1 [128,256), O [256,384), E0 [384,400),
+// E1 [400,416), P [416,432) (eight E2M1 codes per column), P scales
+// [432,440), V scales [440,456) (two buffers), ones' scales 456, Q [480,512).
 // Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
 // drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
 #include "vca_attention_common.cuh"
@@ -43,45 +52,86 @@ using namespace attn;
 
 constexpr int kKStages = 3;                  // K tiles in flight
 constexpr int kRawStages = 4;                // packed V blocks in flight
-constexpr int kVStages = 2;                  // decoded f16 V tiles
-constexpr int kDecWarp0 = 2 + kSoftmaxWarps; // first V-decode warp (its lane 0 also copies)
-constexpr int kDecWarps = 2;                 // two channels per thread
+constexpr int kVStages = 2;                  // swizzled V code tiles
+constexpr int kLayWarp0 = 0;                 // V layout; its lane 0 copies
+constexpr int kLayWarp1 = 2 + kSoftmaxWarps; // V layout
+constexpr int kLayWarps = 2;                 // two channels per thread
+constexpr int kKWarp = kLayWarp1 + 1;        // K producer
 // 12 warps: at most three per SM sub-partition, so up to 168 registers a thread
-constexpr int kThreads = 32 * (kDecWarp0 + kDecWarps);
+constexpr int kThreads = 32 * (kKWarp + 1);
 constexpr int kRsCap = kMeanJ;               // buffered row sums per row
 
 constexpr uint32_t kTileBytes = kBlk * kD;              // one 128 x 128 FP8 K tile
 constexpr uint32_t kCodeBytes = kD * kBlk / 2;          // a block's E2M1 codes, [ch][64 bytes]
 constexpr uint32_t kSfBytes = kD * kBlk / 16;           // a block's E4M3 scales, [ch][8]
 constexpr uint32_t kRawStageBytes = kCodeBytes + kSfBytes;
+constexpr uint32_t kVStageBytes = kD * 128;             // 128 channel rows of 128 bytes (codes in the first 64)
 constexpr uint32_t kOnesRows = 16;
-// A decoded V tile is two K panels (keys 0-63, 64-127) of 128-byte rows (64
-// f16), each [16 rows of 1.0 | 128 channel rows | 16 rows of 1.0].
-constexpr uint32_t kPanelBytes = (kOnesRows + kD + kOnesRows) * 128;
-constexpr uint32_t kVStageBytes = 2 * kPanelBytes;
+constexpr uint32_t kOnesBytes = kOnesRows * 128;        // 16 rows of E2M1 1.0: the row-sum MMA's B
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemE0 = 256, kTmemO = 272, kTmemE1 = 400, kTmemP = 416, kTmemQ = 480;
+constexpr uint32_t kTmemO = 256, kTmemE0 = 384, kTmemE1 = 400, kTmemP = 416, kTmemSFA = 432, kTmemSFB = 440,
+                   kTmemSF1 = 456, kTmemQ = 480;
 
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
-constexpr uint32_t kOffRaw = kOffV + kVStages * kVStageBytes;
-constexpr uint32_t kOffMA = kOffRaw + kRawStages * kRawStageBytes;
+constexpr uint32_t kOffOnes = kOffV + kVStages * kVStageBytes;
+constexpr uint32_t kSfbBytes = 32 * 16;                  // V scales of one MMA: 32 rows x 4 words
+constexpr uint32_t kOffSfb = kOffOnes + kOnesBytes;        // [kVStages][2][kSfbBytes]
+constexpr uint32_t kOffRaw = kOffSfb + kVStages * 2 * kSfbBytes;
+constexpr uint32_t kOffMA = (kOffRaw + kRawStages * kRawStageBytes + 1023) & ~1023u;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
 constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128] buffered row sums
 constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128]: g for every channel
 constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
 constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
 constexpr uint32_t kOffRcp = kOffL + kBlk * 4;              // fp32 [128]: 1 / dec(E4M3 code), 0 for code 0
-constexpr uint32_t kOffSf2 = kOffRcp + kBlk * 4;            // u32 [128]: dec(E4M3 code) as f16 in both halves
-constexpr uint32_t kOffBar = kOffSf2 + kBlk * 4;
+constexpr uint32_t kOffBar = kOffRcp + kBlk * 4;
 constexpr int kNumBars = 1 + 2 * kKStages + 2 + kVStages + 2 * kRawStages + 1 + 2 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
-static_assert(kOffV % 1024 == 0 && kPanelBytes % 1024 == 0 && kOffMA % 1024 == 0 && kOffMB % 1024 == 0,
+static_assert(kOffV % 1024 == 0 && kVStageBytes % 1024 == 0 && kOffOnes % 1024 == 0 && kOffMA % 1024 == 0 &&
+                  kOffMB % 1024 == 0,
               "swizzled operand tiles need 1024-byte alignment");
 static_assert(kRawStageBytes % 16 == 0 && kOffRaw % 16 == 0, "bulk copies need 16-byte alignment");
+static_assert(kOffSfb % 128 == 0, "scale-factor copies start on a 16-byte boundary");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kD % (kDecWarps * 32) == 0, "decode threads cover the channels evenly");
+static_assert(kD % (kLayWarps * 32) == 0, "layout threads cover the channels evenly");
+static_assert(kTmemSF1 < kTmemQ && kTmemSFB + 2 * 8 <= kTmemSF1, "TMEM plan");
+
+// Instruction descriptor of the block-scaled FP4 MMA: A and B E2M1, UE4M3 scale
+// factors (one per 16 elements, scale_vec::4X), scale-factor IDs 0, K = 64.
+__host__ __device__ constexpr uint32_t make_idesc_mxf4(int M, int N) {
+    return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D (+)= A B^T with A (E2M1 codes) in TMEM, B described in shared memory, and
+// the scale factors of A and B in TMEM.
+__device__ __forceinline__ void mma_mxf4_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], [%1], %2, %3, [%4], [%5], p;\n\t}\n"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Shared-memory descriptor of a plain (no swizzle) matrix of 16-byte rows
+// stored one after another: 8-row groups 128 bytes apart.
+__device__ __forceinline__ uint64_t sdesc_rows16(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= static_cast<uint64_t>(16 >> 4) << 16;              // leading byte offset (one 16-byte column)
+    d |= static_cast<uint64_t>(128 >> 4) << 32;             // stride byte offset: next 8 rows
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version for tcgen05
+    return d;                                               // layout type 0: no swizzle
+}
+
+// 32 rows x 128 bits from shared memory into TMEM columns taddr .. taddr + 3,
+// row r into lane r of every lane quarter (asynchronous, ordered before the
+// MMAs this thread issues after it).
+__device__ __forceinline__ void tc_cp_rows_x4(uint32_t taddr, uint64_t sdesc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
 
 struct Bars {
     uint64_t *q_full, *k_full, *k_empty, *s_ready, *v_full, *raw_full, *raw_empty, *p_full, *pv_done, *drain;
@@ -102,52 +152,22 @@ struct Params {
 // stages its operands in step j, once block j-1's row sums are read.
 __host__ __device__ constexpr bool flush_after(int j) { return j >= kMeanJ && (j % kMeanJ) == 0; }
 
-__device__ __forceinline__ uint32_t f16x2_mul(uint32_t a, uint32_t b) {
-    uint32_t d;
-    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-    return d;
-}
-
-// f16 pattern of an E4M3 byte, in both halves of a word.
-__device__ __forceinline__ uint32_t e4m3_f16x2_splat(uint32_t code) {
-    const uint32_t h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(code), __NV_E4M3).x;
-    return h | (h << 16);
-}
-
-// The four bytes of w, each two E2M1 nibbles -> f16x2 (the low nibble in the
-// low half): d[i] from byte i.
-__device__ __forceinline__ void e2m1x8_f16x2(uint32_t w, uint32_t &d0, uint32_t &d1, uint32_t &d2, uint32_t &d3) {
-    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\tmov.b32 {b0, b1, b2, b3}, %4;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\tcvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
-        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\tcvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
-        : "=r"(d0), "=r"(d1), "=r"(d2), "=r"(d3)
-        : "r"(w));
-}
-
-// (lo, hi) rounded to E2M1 (nearest even, saturating at 6) and decoded back,
-// as f16x2 (lo in the low half).
-__device__ __forceinline__ uint32_t e2m1_round_f16x2(float lo, float hi) {
-    uint32_t d;
-    asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %2, %1;\n\tcvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-        : "=r"(d)
-        : "f"(lo), "f"(hi));
-    return d;
-}
-
 // NVFP4 P of this thread's kCols keys against the reference max m: per group
 // of 16 keys p = 2^(fma(S, c, -m)), scale sf = E4M3(amax16 / 6), code =
-// E2M1(p * (1 / dec(sf))), decoded value code * dec(sf) as f16 (exact), two
-// keys per word.  amax16 / 6 is the quotient corrected by one FMA step,
+// E2M1(p * (1 / dec(sf))); P gets the codes (key k of the thread's keys at
+// word k / 8, nibble k % 8), sfa the four scale bytes (group g in byte g).
+// amax16 / 6 is the quotient corrected by one FMA step,
 // q = RN(a r), q' = RN(q + RN(a - 6q) r) with r = RN(1/6): equal to the IEEE
 // quotient for every a in [2^-120, 2^30] (checked exhaustively), and below
-// that both round to the E4M3 code 0.  The reciprocal and the f16 pattern of
-// the scale come from per-CTA tables of the 127 codes (sRcp, sSf2).
+// that both round to the E4M3 code 0.  The reciprocal of the scale comes from
+// a per-CTA table of the 127 codes (sRcp).
 __device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], float c, float m, const float *sRcp,
-                                        const uint32_t *sSf2, uint32_t (&P)[kCols / 2]) {
+                                        uint32_t (&P)[kCols / 8], uint32_t &sfa) {
     constexpr float kSixth = 1.0f / 6.0f;
     const float negm = -m;
     const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
     const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
+    sfa = 0u;
 #pragma unroll
     for (int g = 0; g < kCols / 16; ++g) {
         float pv[16];
@@ -165,14 +185,16 @@ __device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], float c, flo
         const float q0 = __fmul_rn(amax, kSixth);
         const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), kSixth, q0);
         const uint32_t sf = e4m3x2(q1, 0.0f) & 0xFFu;
+        sfa |= sf << (8 * g);
         const float inv = sRcp[sf];
-        const uint32_t sf2 = sSf2[sf];
         const uint64_t inv2 = pk2(__float_as_uint(inv), __float_as_uint(inv));
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float x0, x1;
-            upk2(mul2(pk2(__float_as_uint(pv[2 * q]), __float_as_uint(pv[2 * q + 1])), inv2), x0, x1);
-            P[8 * g + q] = f16x2_mul(e2m1_round_f16x2(x0, x1), sf2);
+        for (int w = 0; w < 2; ++w) {
+            float x[8];
+#pragma unroll
+            for (int q = 0; q < 8; q += 2)
+                upk2(mul2(pk2(__float_as_uint(pv[8 * w + q]), __float_as_uint(pv[8 * w + q + 1])), inv2), x[q], x[q + 1]);
+            P[2 * g + w] = e2m1x8(x);
         }
     }
 }
@@ -201,7 +223,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sPM = reinterpret_cast<float *>(smem + kOffPM);
     float *sL = reinterpret_cast<float *>(smem + kOffL);
     float *sRcp = reinterpret_cast<float *>(smem + kOffRcp);
-    uint32_t *sSf2 = reinterpret_cast<uint32_t *>(smem + kOffSf2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qtile = blockIdx.x, bh = blockIdx.y;
@@ -217,10 +238,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(B.s_ready + i, 1);
             mbar_init(B.pv_done + i, 1);
         }
-        for (int i = 0; i < kVStages; ++i) mbar_init(B.v_full + i, kDecWarps);
+        for (int i = 0; i < kVStages; ++i) mbar_init(B.v_full + i, kLayWarps);
         for (int s = 0; s < kRawStages; ++s) {
             mbar_init(B.raw_full + s, 1);
-            mbar_init(B.raw_empty + s, kDecWarps);
+            mbar_init(B.raw_empty + s, kLayWarps);
         }
         mbar_init(B.p_full, kSoftmaxWarps);
         mbar_init(B.drain, 1);
@@ -236,15 +257,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         sSV[t] = p.v_scale[bh];
         // scale tables for the E4M3 codes (127 = NaN is never produced)
         sRcp[t] = (t == 0 || t == 127) ? 0.0f : __frcp_rn(e4m3_to_f32(static_cast<uint32_t>(t)));
-        sSf2[t] = e4m3_f16x2_splat(static_cast<uint32_t>(t));
-        // the rows of f16 1.0 at both ends of every panel
-        const uint4 ones = make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
-        for (int st = 0; st < kVStages; ++st)
-            for (int pn = 0; pn < 2; ++pn) {
-                unsigned char *panel = smem + kOffV + st * kVStageBytes + pn * kPanelBytes;
-                *reinterpret_cast<uint4 *>(panel + 16 * t) = ones;
-                *reinterpret_cast<uint4 *>(panel + (kOnesRows + kD) * 128 + 16 * t) = ones;
-            }
+        // the row-sum MMA's B: 16 rows of E2M1 1.0 (every nibble 2)
+        const uint4 ones = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
+        *reinterpret_cast<uint4 *>(smem + kOffOnes + 16 * t) = ones;
         fence_proxy_async_smem();
     }
     tc_fence_before();
@@ -252,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
+    if (warp == kKWarp) {
         // ------------------------------------------------------------ K producer
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
@@ -268,17 +283,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int s = 0; s < kKStages; ++s)
                 if (armed[s] > 0) drain_wait(B.k_full + s, (armed[s] - 1) & 1, p.limit_ns);
         }
-    } else if (warp >= kDecWarp0) {
-        // ------------------------------------------------------------ V decode
-        // Per channel ch: 128 E2M1 codes (token 2i in the low nibble of byte
-        // i) and 8 E4M3 scales -> 128 f16 values, written as 16-byte chunks
-        // (8 keys) of row 16 + ch of the two K panels.
-        const int t0 = threadIdx.x - 32 * kDecWarp0;
-        const bool copier = (warp == kDecWarp0 && lane == 0);
+    } else if (warp == kLayWarp0 || warp == kLayWarp1) {
+        // ------------------------------------------------------------ V layout
+        // Per channel ch: the 64 bytes of its 128 E2M1 codes (token 2i in the
+        // low nibble of byte i) as the first four 16-byte chunks of row ch of
+        // the swizzled tile.  The block's V scales are staged for the MMA
+        // issuer's copy into TMEM: for keys 64h.. (MMA h), row r of matrix
+        // (v, h) holds the four scales of channels r, r + 32, r + 64, r + 96
+        // (the MMA reads channel n's from lane n % 32 of the D row's lane
+        // quarter, column n / 32).
+        const bool lanes0 = warp == kLayWarp0;
+        const int t0 = (lanes0 ? 0 : 32) + lane;
+        const bool copier = (lanes0 && lane == 0);
         int armed[kRawStages];
         for (int s = 0; s < kRawStages; ++s) armed[s] = 0;
         // block b's codes and scales into raw stage b % kRawStages, which the
-        // decode of block b - kRawStages (both warps) has released
+        // layout of block b - kRawStages (both warps) has released
         auto copy_block = [&](int b) -> bool {
             const int s = b % kRawStages, use = b / kRawStages;
             if (use > 0 && !mbar_wait(B.raw_empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) return false;
@@ -297,39 +317,27 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int s = j % kRawStages, v = j & 1;
             if (copier && cok && j + kRawStages - 1 < nb) cok = copy_block(j + kRawStages - 1);
             bool ok = cok && mbar_wait(B.raw_full + s, (j / kRawStages) & 1, abort_flag, p.limit_ns);
-            // decoded stage v was last read by PV(j-2)
+            // tile v and the V-scale buffer v were last read by PV(j-2)
             if (ok && j >= 2) ok = mbar_wait(B.pv_done + (j & 1), ((j - 2) >> 1) & 1, abort_flag, p.limit_ns);
             if (!__all_sync(0xffffffffu, ok)) break;
             const unsigned char *raw = smem + kOffRaw + s * kRawStageBytes;
             unsigned char *vs = smem + kOffV + v * kVStageBytes;
-#pragma unroll 1
-            for (int t = t0; t < kD; t += 32 * kDecWarps) {
-                uint32_t code[16];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint4 u = reinterpret_cast<const uint4 *>(raw + t * (kBlk / 2))[i];
-                    code[4 * i] = u.x;
-                    code[4 * i + 1] = u.y;
-                    code[4 * i + 2] = u.z;
-                    code[4 * i + 3] = u.w;
-                }
-                const uint2 sfw = *reinterpret_cast<const uint2 *>(raw + kCodeBytes + t * (kBlk / 16));
+            for (int t = t0; t < kD; t += 32 * kLayWarps) {
 #pragma unroll
-                for (int g = 0; g < kBlk / 16; ++g) {
-                    const uint32_t sf2 = e4m3_f16x2_splat(((g < 4 ? sfw.x : sfw.y) >> (8 * (g & 3))) & 0xFFu);
-#pragma unroll
-                    for (int h = 0; h < 2; ++h) {
-                        const uint32_t w = code[2 * g + h];   // keys 16g + 8h .. +7
-                        uint4 o;
-                        e2m1x8_f16x2(w, o.x, o.y, o.z, o.w);
-                        o.x = f16x2_mul(o.x, sf2);
-                        o.y = f16x2_mul(o.y, sf2);
-                        o.z = f16x2_mul(o.z, sf2);
-                        o.w = f16x2_mul(o.w, sf2);
-                        const int panel = g >> 2, chunk = (2 * g + h) & 7;
-                        *reinterpret_cast<uint4 *>(vs + panel * kPanelBytes + sw128_offset(kOnesRows + t, chunk)) = o;
-                    }
-                }
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4 *>(vs + sw128_offset(t, i)) =
+                        reinterpret_cast<const uint4 *>(raw + t * (kBlk / 2))[i];
+            }
+            {
+                const int h = t0 >> 5;   // thread t0 stages row lane of matrix (v, h)
+                const unsigned char *sf = raw + kCodeBytes + 4 * h;
+                uint4 w;
+                w.x = *reinterpret_cast<const uint32_t *>(sf + (lane + 0) * (kBlk / 16));
+                w.y = *reinterpret_cast<const uint32_t *>(sf + (lane + 32) * (kBlk / 16));
+                w.z = *reinterpret_cast<const uint32_t *>(sf + (lane + 64) * (kBlk / 16));
+                w.w = *reinterpret_cast<const uint32_t *>(sf + (lane + 96) * (kBlk / 16));
+                *reinterpret_cast<uint4 *>(smem + kOffSfb + (2 * v + h) * kSfbBytes + 16 * lane) = w;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(B.raw_empty + s);
@@ -345,7 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc(128, 128, 0, 0);    // E4M3 x E4M3
-            constexpr uint32_t idesc_pv = make_idesc(128, 144, 0, 0);    // F16 x F16
+            constexpr uint32_t idesc_pv = make_idesc_mxf4(128, 128);     // NVFP4 x NVFP4
+            constexpr uint32_t idesc_rs = make_idesc_mxf4(128, kOnesRows);
             constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);  // BF16 x BF16
             const uint32_t sbase = smem_u32(smem);
             const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
@@ -368,15 +377,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int b = 0; ok && b < 2 && b < nb; ++b) ok = issue_qk(b);
             for (int j = 0; ok && j < nb; ++j) {
                 if (!mbar_wait(B.v_full + (j & 1), (j >> 1) & 1, abort_flag, p.limit_ns)) break;
+                tc_fence_after();
+                // block j's V scales into every lane quarter (buffer j & 1 was
+                // last read by PV(j-2), which finished before tile j was laid out)
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tc_cp_rows_x4(tmem + kTmemSFB + 8 * (j & 1) + 4 * h,
+                                  sdesc_rows16(sbase + kOffSfb + (2 * (j & 1) + h) * kSfbBytes));
                 if (!mbar_wait(B.p_full, j & 1, abort_flag, p.limit_ns)) break;
                 tc_fence_after();
-                // even j: B = [ones ; V], D = [E0 | O]; odd j: B = [V ; ones], D = [O | E1]
-                const uint32_t vstage = sbase + kOffV + (j & 1) * kVStageBytes + ((j & 1) ? kOnesRows * 128 : 0);
-                const uint32_t td = tmem + ((j & 1) ? kTmemO : kTmemE0);
+                // O += P V and E_{j&1} = P ones, keys 64h .. 64h+63 per MMA
+                // (A columns 8h.., B bytes 32h.. of every row, scales at +4h)
+                const uint64_t dv = sdesc_k_sw128(sbase + kOffV + (j & 1) * kVStageBytes);
+                const uint64_t d1 = sdesc_k_sw128(sbase + kOffOnes);
+                const uint32_t te = tmem + ((j & 1) ? kTmemE1 : kTmemE0);
 #pragma unroll
-                for (int kk = 0; kk < kBlk / 16; ++kk)
-                    mma_f16_ts(td, tmem + kTmemP + 8 * kk, sdesc_k_sw128(vstage + (kk >> 2) * kPanelBytes) + 2 * (kk & 3),
-                               idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                for (int h = 0; h < 2; ++h)
+                    mma_mxf4_ts(tO, tmem + kTmemP + 8 * h, dv + 2 * h, idesc_pv, tmem + kTmemSFA + 4 * h,
+                                tmem + kTmemSFB + 8 * (j & 1) + 4 * h, (j > 0 || h > 0) ? 1u : 0u);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    mma_mxf4_ts(te, tmem + kTmemP + 8 * h, d1 + 2 * h, idesc_rs, tmem + kTmemSFA + 4 * h, tmem + kTmemSF1,
+                                h > 0 ? 1u : 0u);
                 if (flush_after(j)) {
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
@@ -396,7 +418,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
         const uint32_t col0 = static_cast<uint32_t>(kCols) * half;
         const uint32_t tO = tmem + lane_base + kTmemO + col0;
-        const uint32_t tP = tmem + lane_base + kTmemP + (kCols / 2) * half;
+        const uint32_t tP = tmem + lane_base + kTmemP + (kCols / 8) * half;       // this half's codes
+        // its scales: the MMA reads row m's from lane m, column base + m / 32
+        const uint32_t tSFA = tmem + lane_base + kTmemSFA + 4 * half + quarter;
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
         const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
@@ -411,6 +435,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (half == 0) {
             load_q_row(p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD,
                        tmem + lane_base + kTmemQ);
+            // the row-sum MMA's B scales (E4M3 1.0), read in every lane quarter
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tmem + lane_base + kTmemSF1),
+                         "r"(0x38383838u) : "memory");
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -446,8 +473,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
                 m = bm;
             }
-            uint32_t P[kCols / 2];
-            nvfp4_p(S, c, m, sRcp, sSf2, P);
+            uint32_t P[kCols / 8], sfa;
+            nvfp4_p(S, c, m, sRcp, P, sfa);
             // PV(b-1) is done: the P buffer and O are free, block b-1's row sums
             // are in their slot
             if (b >= 1) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + ((b - 1) & 1), ((b - 1) >> 1) & 1, abort_flag,
@@ -456,15 +483,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if (half == 0 && b >= 1) {
                     // read block b-1's sums (taken against the max before this
-                    // block's update) and clear this block's slot for PV(b)
+                    // block's update); PV(b)'s row-sum MMA overwrites this
+                    // block's slot
                     const uint32_t te_prev = tmem + lane_base + (sb ? kTmemE0 : kTmemE1);
-                    const uint32_t te_cur = tmem + lane_base + (sb ? kTmemE1 : kTmemE0);
                     uint32_t rs_raw;
                     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te_prev));
                     tmem_ld_wait();
-                    asm volatile(
-                        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"
-                        ::"r"(te_cur), "r"(0u) : "memory");
                     const float rs = __uint_as_float(rs_raw);
                     l = __fadd_rn(l, rs);
                     sRS[rs_cnt * kBlk + row] = rs;
@@ -492,7 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rs_cnt = 0;
                     fence_proxy_async_smem();   // the mean operands are read by the tensor core
                 }
-                VCA_TMEM_ST32(tP, P);
+                VCA_TMEM_ST8(tP, P);
+                asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tSFA), "r"(sfa) : "memory");
                 tmem_st_wait();
                 tc_fence_before();
                 __syncwarp();

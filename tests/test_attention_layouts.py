@@ -26,6 +26,7 @@ def constants(*files):
             for part in m.group(1).split(","):
                 name, _, expr = part.partition("=")
                 expr = re.sub(r"//.*", "", expr).replace("/", "//").strip()
+                expr = re.sub(r"\b(\d+)u\b", r"\1", expr)   # unsigned literals
                 try:
                     env[name.strip()] = int(eval(expr, {"__builtins__": {}}, dict(env)))
                 except (NameError, SyntaxError):
@@ -86,26 +87,39 @@ def test_e4m3_shared_memory_layout(e4m3):
 
 
 def test_nvfp4_tmem_plan(nvfp4):
+    """The 4-bit kernel's columns: P as E2M1 codes (128 keys at eight per
+    column), its scales (two MMAs x four lane-quarter columns), V's scales
+    (two buffers x two MMAs x four columns of lanes 0-31) and the ones rows'
+    scale column, none overlapping S, O, the row-sum slots or Q."""
     c = nvfp4
-    cols = {"S0": (0, 128), "S1": (128, 256), "E0": (c["kTmemE0"], c["kTmemE0"] + 16),
-            "O": (c["kTmemO"], c["kTmemO"] + 128), "E1": (c["kTmemE1"], c["kTmemE1"] + 16),
-            "P": (c["kTmemP"], c["kTmemP"] + 64), "Q": (c["kTmemQ"], c["kTmemQ"] + 32)}
+    cols = {"S0": (0, 128), "S1": (128, 256), "O": (c["kTmemO"], c["kTmemO"] + 128),
+            "E0": (c["kTmemE0"], c["kTmemE0"] + 16), "E1": (c["kTmemE1"], c["kTmemE1"] + 16),
+            "P": (c["kTmemP"], c["kTmemP"] + 128 // 8), "SFA": (c["kTmemSFA"], c["kTmemSFA"] + 2 * 4),
+            "SFB": (c["kTmemSFB"], c["kTmemSFB"] + 2 * 2 * 4), "SF1": (c["kTmemSF1"], c["kTmemSF1"] + 1),
+            "Q": (c["kTmemQ"], c["kTmemQ"] + 32)}
     _disjoint(cols, c["kTmemCols"])
-    assert c["kTmemE0"] + 16 == c["kTmemO"] and c["kTmemO"] + 128 == c["kTmemE1"]
+    # the row-sum MMA writes N = 16 columns into a slot of 16
+    assert c["kOnesRows"] == 16
 
 
 def test_nvfp4_shared_memory_layout(nvfp4):
     c = nvfp4
     assert c["kThreads"] == 384
+    assert c["kVStageBytes"] == 128 * 128                                      # a channel row of 128 bytes
     for s in range(c["kVStages"]):
-        for panel in range(2):
-            assert (c["kOffV"] + s * c["kVStageBytes"] + panel * c["kPanelBytes"]) % 1024 == 0
+        assert (c["kOffV"] + s * c["kVStageBytes"]) % 1024 == 0                # swizzled B tiles
+    assert c["kOffOnes"] % 1024 == 0 and c["kOnesBytes"] == 16 * 128
     assert c["kOffMA"] % 1024 == 0 and c["kOffMB"] % 1024 == 0
+    # the V-scale matrices the MMA issuer copies into TMEM: 32 rows of 16 bytes,
+    # one per stage and 64-key half, on 16-byte boundaries
+    assert c["kSfbBytes"] == 32 * 16 and c["kOffSfb"] % 16 == 0
+    assert c["kOffSfb"] >= c["kOffOnes"] + c["kOnesBytes"]
+    assert c["kOffSfb"] + c["kVStages"] * 2 * c["kSfbBytes"] <= c["kOffRaw"]
     for s in range(c["kRawStages"]):
         assert (c["kOffRaw"] + s * c["kRawStageBytes"]) % 16 == 0                 # bulk copy destinations
     assert c["kOffBar"] % 8 == 0 and c["kSmemBytes"] <= 232448
-    order = ["kOffK", "kOffV", "kOffRaw", "kOffMA", "kOffMB", "kOffRS", "kOffSV", "kOffPM", "kOffL", "kOffRcp",
-             "kOffSf2", "kOffBar", "kOffMisc"]
+    order = ["kOffK", "kOffV", "kOffOnes", "kOffSfb", "kOffRaw", "kOffMA", "kOffMB", "kOffRS", "kOffSV", "kOffPM", "kOffL",
+             "kOffRcp", "kOffBar", "kOffMisc"]
     offs = [c[k] for k in order]
     assert offs == sorted(offs)
 
@@ -115,4 +129,4 @@ def test_the_evaluator_reads_the_sources(e4m3, nvfp4):
     and have the values the kernels' comments state."""
     assert e4m3["kBlk"] == 128 and e4m3["kD"] == 128 and e4m3["kMeanJ"] == 16 and e4m3["kRsSlots"] == 32
     assert e4m3["kOnesBytes"] == 2048 and e4m3["kVStageBytes"] == 2048 + 16384 + 2048
-    assert nvfp4["kCodeBytes"] == 8192 and nvfp4["kSfBytes"] == 1024 and nvfp4["kPanelBytes"] == 160 * 128
+    assert nvfp4["kCodeBytes"] == 8192 and nvfp4["kSfBytes"] == 1024 and nvfp4["kOnesBytes"] == 2048

@@ -36,13 +36,13 @@ def test_peaks_from_the_measured_rates(bench):
     fp8, src = bench.attention_peak("e4m3", peaks)
     assert fp8 == pytest.approx(3901.2) and "burst" in src
     fp4, _ = bench.attention_peak("nvfp4", peaks)
-    # QK at the FP8 rate (2b), PV on f16 operands at b: 1 / (0.5 / 2b + 0.5 / b)
-    assert fp4 == pytest.approx(1.0 / (0.5 / 3901.2 + 0.5 / 1950.6))
+    # QK at the FP8 rate (2b), PV as the block-scaled FP4 MMA at 6b: 1 / (0.5 / 2b + 0.5 / 6b)
+    assert fp4 == pytest.approx(1.0 / (0.5 / 3901.2 + 0.5 / (6 * 1950.6)))
     fallback, src = bench.attention_peak("e4m3", None)
     assert fallback == pytest.approx(3800.0) and "fallback" in src
-    # against nominal dense rates: FP8 4.5 PF; the NVFP4 kernel's QK at FP8, PV at bf16
+    # against nominal dense rates: FP8 4.5 PF; the NVFP4 kernel's QK at FP8, PV at FP4 13.5 PF
     assert bench.attention_nominal("e4m3") == pytest.approx(4500.0)
-    assert bench.attention_nominal("nvfp4") == pytest.approx(1.0 / (0.5 / 4500.0 + 0.5 / 2250.0))
+    assert bench.attention_nominal("nvfp4") == pytest.approx(1.0 / (0.5 / 4500.0 + 0.5 / 13500.0))
 
 
 def test_algorithmic_bytes(bench):
