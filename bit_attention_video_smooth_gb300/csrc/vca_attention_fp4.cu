@@ -84,8 +84,8 @@ constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128
 constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128]: g for every channel
 constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
 constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
-constexpr uint32_t kOffRcp = kOffL + kBlk * 4;              // fp32 [128]: 1 / dec(E4M3 code), 0 for code 0
-constexpr uint32_t kOffBar = kOffRcp + kBlk * 4;
+constexpr uint32_t kOffLg = kOffL + kBlk * 4;               // fp32 [128]: -log2(dec(E4M3 code)), -inf for code 0
+constexpr uint32_t kOffBar = kOffLg + kBlk * 4;
 constexpr int kNumBars = 1 + 2 * kKStages + 2 + kVStages + 2 * kRawStages + 1 + 2 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
@@ -152,48 +152,58 @@ struct Params {
 // stages its operands in step j, once block j-1's row sums are read.
 __host__ __device__ constexpr bool flush_after(int j) { return j >= kMeanJ && (j % kMeanJ) == 0; }
 
+// Largest raw score of each group of 16 of the thread's kCols keys.
+__device__ __forceinline__ void group_max(const uint32_t (&S)[kCols], float (&gm)[kCols / 16]) {
+#pragma unroll
+    for (int g = 0; g < kCols / 16; ++g) {
+        const uint32_t *s = S + 16 * g;
+        const float a = max3(__uint_as_float(s[0]), __uint_as_float(s[1]), __uint_as_float(s[2]));
+        const float b = max3(__uint_as_float(s[3]), __uint_as_float(s[4]), __uint_as_float(s[5]));
+        const float c = max3(__uint_as_float(s[6]), __uint_as_float(s[7]), __uint_as_float(s[8]));
+        const float d = max3(__uint_as_float(s[9]), __uint_as_float(s[10]), __uint_as_float(s[11]));
+        const float e = max3(__uint_as_float(s[12]), __uint_as_float(s[13]), __uint_as_float(s[14]));
+        gm[g] = fmaxf(max3(a, b, c), max3(d, e, __uint_as_float(s[15])));
+    }
+}
+
 // NVFP4 P of this thread's kCols keys against the reference max m: per group
 // of 16 keys p = 2^(fma(S, c, -m)), scale sf = E4M3(amax16 / 6), code =
-// E2M1(p * (1 / dec(sf))); P gets the codes (key k of the thread's keys at
-// word k / 8, nibble k % 8), sfa the four scale bytes (group g in byte g).
-// amax16 / 6 is the quotient corrected by one FMA step,
+// E2M1(p / dec(sf)); P gets the codes (key k of the thread's keys at word
+// k / 8, nibble k % 8), sfa the four scale bytes (group g in byte g).
+// With c > 0, S -> 2^(fma(S, c, -m)) does not decrease, so amax16 is 2 to
+// the power of the group's largest score term (gm, from group_max).  The
+// quotient amax16 / 6 is corrected by one FMA step,
 // q = RN(a r), q' = RN(q + RN(a - 6q) r) with r = RN(1/6): equal to the IEEE
 // quotient for every a in [2^-120, 2^30] (checked exhaustively), and below
-// that both round to the E4M3 code 0.  The reciprocal of the scale comes from
-// a per-CTA table of the 127 codes (sRcp).
-__device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], float c, float m, const float *sRcp,
-                                        uint32_t (&P)[kCols / 8], uint32_t &sfa) {
+// that both round to the E4M3 code 0.  p / dec(sf) is evaluated as
+// 2^(fma(S, c, lg(sf) - m)) with lg(sf) = -log2(dec(sf)) from a per-CTA
+// table of the 127 codes (sLg; -inf for code 0, whose group codes are 0):
+// one FMA and one exp per key, the same hardware-exp accuracy as p itself.
+__device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], const float (&gm)[kCols / 16], float c, float m,
+                                        const float *sLg, uint32_t (&P)[kCols / 8], uint32_t &sfa) {
     constexpr float kSixth = 1.0f / 6.0f;
     const float negm = -m;
     const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
-    const uint64_t nx2 = pk2(__float_as_uint(negm), __float_as_uint(negm));
     sfa = 0u;
 #pragma unroll
     for (int g = 0; g < kCols / 16; ++g) {
-        float pv[16];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            float t0, t1;
-            upk2(fma2(pk2(S[16 * g + 2 * q], S[16 * g + 2 * q + 1]), cx2, nx2), t0, t1);
-            pv[2 * q] = ex2_approx(t0);
-            pv[2 * q + 1] = ex2_approx(t1);
-        }
-        float a[4] = {pv[0], pv[1], pv[2], pv[3]};
-#pragma unroll
-        for (int j = 4; j < 16; j += 2) a[(j >> 1) & 3] = max3(a[(j >> 1) & 3], pv[j], pv[j + 1]);
-        const float amax = fmaxf(max3(a[0], a[1], a[2]), a[3]);
+        const float amax = ex2_approx(__fmaf_rn(gm[g], c, negm));
         const float q0 = __fmul_rn(amax, kSixth);
         const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), kSixth, q0);
         const uint32_t sf = e4m3x2(q1, 0.0f) & 0xFFu;
         sfa |= sf << (8 * g);
-        const float inv = sRcp[sf];
-        const uint64_t inv2 = pk2(__float_as_uint(inv), __float_as_uint(inv));
+        const float bias = __fadd_rn(sLg[sf], negm);
+        const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
 #pragma unroll
         for (int w = 0; w < 2; ++w) {
             float x[8];
 #pragma unroll
-            for (int q = 0; q < 8; q += 2)
-                upk2(mul2(pk2(__float_as_uint(pv[8 * w + q]), __float_as_uint(pv[8 * w + q + 1])), inv2), x[q], x[q + 1]);
+            for (int q = 0; q < 8; q += 2) {
+                float t0, t1;
+                upk2(fma2(pk2(S[16 * g + 8 * w + q], S[16 * g + 8 * w + q + 1]), cx2, bx2), t0, t1);
+                x[q] = ex2_approx(t0);
+                x[q + 1] = ex2_approx(t1);
+            }
             P[2 * g + w] = e2m1x8(x);
         }
     }
@@ -222,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *sSV = reinterpret_cast<float *>(smem + kOffSV);
     float *sPM = reinterpret_cast<float *>(smem + kOffPM);
     float *sL = reinterpret_cast<float *>(smem + kOffL);
-    float *sRcp = reinterpret_cast<float *>(smem + kOffRcp);
+    float *sLg = reinterpret_cast<float *>(smem + kOffLg);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int qtile = blockIdx.x, bh = blockIdx.y;
@@ -256,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int t = threadIdx.x - 64;
         sSV[t] = p.v_scale[bh];
         // scale tables for the E4M3 codes (127 = NaN is never produced)
-        sRcp[t] = (t == 0 || t == 127) ? 0.0f : __frcp_rn(e4m3_to_f32(static_cast<uint32_t>(t)));
+        sLg[t] = (t == 0 || t == 127) ? __int_as_float(0xff800000) : -log2f(e4m3_to_f32(static_cast<uint32_t>(t)));
         // the row-sum MMA's B: 16 rows of E2M1 1.0 (every nibble 2)
         const uint4 ones = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
         *reinterpret_cast<uint4 *>(smem + kOffOnes + 16 * t) = ones;
@@ -451,6 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool wok = mbar_wait(B.s_ready + sb, (b >> 1) & 1, abort_flag, p.limit_ns);
             wok = __all_sync(0xffffffffu, wok) && ok;
             uint32_t S[kCols];
+            float gm[kCols / 16];
             float pm = kNegInf;
             if (wok) {
                 tc_fence_after();
@@ -458,7 +469,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S + 32 * i));
                 tmem_ld_wait();
-                pm = row_part_max(S);
+                group_max(S, gm);
+                pm = gm[0];
+#pragma unroll
+                for (int g = 1; g < kCols / 16; ++g) pm = fmaxf(pm, gm[g]);
                 sPM[(sb * kParts + half) * kBlk + row] = pm;
             }
             ok = bar_and(wok, pair_bar, 32 * kParts);
@@ -474,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 m = bm;
             }
             uint32_t P[kCols / 8], sfa;
-            nvfp4_p(S, c, m, sRcp, P, sfa);
+            nvfp4_p(S, gm, c, m, sLg, P, sfa);
             // PV(b-1) is done: the P buffer and O are free, block b-1's row sums
             // are in their slot
             if (b >= 1) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + ((b - 1) & 1), ((b - 1) >> 1) & 1, abort_flag,

@@ -119,7 +119,7 @@ def test_nvfp4_shared_memory_layout(nvfp4):
         assert (c["kOffRaw"] + s * c["kRawStageBytes"]) % 16 == 0                 # bulk copy destinations
     assert c["kOffBar"] % 8 == 0 and c["kSmemBytes"] <= 232448
     order = ["kOffK", "kOffV", "kOffOnes", "kOffSfb", "kOffRaw", "kOffMA", "kOffMB", "kOffRS", "kOffSV", "kOffPM", "kOffL",
-             "kOffRcp", "kOffBar", "kOffMisc"]
+             "kOffLg", "kOffBar", "kOffMisc"]
     offs = [c[k] for k in order]
     assert offs == sorted(offs)
 
