@@ -69,7 +69,6 @@ constexpr uint32_t kTmemCols = 512;
 // PV of an even block writes [E0 | O] (B = [ones ; V]), of an odd block [O | E1]
 // (B = [V ; ones]): the 16 extra output columns are the block's row sums.
 constexpr uint32_t kTmemE0 = 256, kTmemO = 272, kTmemE1 = 400, kTmemP0 = 416, kTmemQ = 480;
-constexpr uint32_t kBarHand0 = 2;          // + 2 * quarter + parity: the reference-max hand-over
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t kOffK = 0;
@@ -107,16 +106,6 @@ struct Params {
     uint32_t one;   // 1: an opaque multiplier for integer adds on the FMA pipe
 };
 
-// A mean-restore MMA follows PV(b) for b = 19, 35, 51, ...: it adds the terms
-// of blocks b-19 .. b-4.  Their row sums are all visible to the thread that
-// stages them at block b (b is odd, so that thread takes the odd blocks): the
-// sum of an odd block j is written by the thread itself at block j+2 <= b-2,
-// the sum of an even block j <= b-5 by its partner at block j+2, before the
-// partner hands over the reference max at block j+4 <= b-1.
-constexpr int kMeanLag = 3;
-__host__ __device__ constexpr bool flush_after(int b) {
-    return b >= kMeanJ + kMeanLag && (b % kMeanJ) == kMeanLag;
-}
 
 // exp2 then E4M3 for four raw scores: p = 2^(fma(S, c, -m)).
 __device__ __forceinline__ uint32_t expconv4(uint64_t s01, uint64_t s23, uint64_t cx2, uint64_t negmx2) {
@@ -174,28 +163,6 @@ __device__ __forceinline__ void codes32(const uint32_t (&X)[kCols], float c, flo
     }
 }
 
-// Operands of the mean-restore MMA for blocks b0 .. b0+15 (row / channel
-// `row`): A row = the row sums from their ring slots, each brought from the
-// reference max it was taken against to m; B row = mean / s_v.
-__device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
-                                            const uint16_t *sMeanGroup, const float *sSV, unsigned char *sMA,
-                                            unsigned char *sMB) {
-    float hi[kMeanJ], lo[kMeanJ];
-#pragma unroll
-    for (int i = 0; i < kMeanJ; ++i) {
-        const int slot = ((b0 + i) & (kRsSlots - 1)) * kBlk + row;
-        float rs = sRS[slot];
-        const float mt = sRSM[slot];
-        if (mt != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mt, m)));
-        split_bf16(rs, hi[i], lo[i]);
-    }
-    store_mean_row(sMA, row, hi, lo, true);
-    const float inv_sv = 1.0f / sSV[row];
-#pragma unroll
-    for (int i = 0; i < kMeanJ; ++i)
-        split_bf16(__fmul_rn(bf16_bits_to_f32(sMeanGroup[i * kD + row]), inv_sv), hi[i], lo[i]);
-    store_mean_row(sMB, row, hi, lo, false);
-}
 
 template <bool kExpcast>
 __global__ void __launch_bounds__(kThreads, 1)

@@ -18,10 +18,9 @@
 namespace vca {
 namespace attn {
 
-// Eight softmax warps, two per TMEM lane quarter.  The NVFP4 kernel splits a
-// row's S columns between the two (column halves); the 8-bit kernel gives
-// them alternate key blocks and holds a row in registers kCols columns at a
-// time.
+// Eight softmax warps, two per TMEM lane quarter: the two take alternate key
+// blocks (one thread per query row and block) and hold a row in registers
+// kCols columns at a time.
 constexpr int kParts = 2;
 constexpr int kCols = kBlk / kParts;       // S columns held in registers at a time
 constexpr int kSoftmaxWarps = 4 * kParts;
@@ -29,7 +28,7 @@ constexpr int kMeanJ = 16;                 // key blocks per mean-restore MMA
 constexpr float kLazyTau = 8.0f;           // log2 units: the reference max moves by more than 2^8 only
 
 constexpr uint32_t kBarSoftmax = 1;        // all softmax warps
-constexpr uint32_t kBarPair0 = 2;          // + quarter: the two warps of one TMEM lane quarter (NVFP4 kernel)
+constexpr uint32_t kBarHand0 = 2;          // + 2 * quarter + parity: the reference-max hand-over
 
 // Wait ignoring the abort flag (used only to drain work this thread issued).
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity, uint64_t limit_ns) {
@@ -97,25 +96,6 @@ __device__ __forceinline__ void store_mean_row(unsigned char *dst, int row, cons
     }
 }
 
-// Operands of one mean-restore MMA for key blocks b0 .. b0+kMeanJ-1, written
-// by the two threads of query row / channel `row`:
-//   half 0: A row `row` (query row) = [rs hi | rs lo | rs hi | rs lo] from sRS
-//   half 1: B row `row` (channel)   = [mu hi | mu hi | mu lo | mu lo], mu = mean / s_v
-// into the 128-byte-swizzled K-major tiles sMA / sMB.
-__device__ __forceinline__ void stage_mean_operands(int half, int row, const float *sRS, const uint16_t *vmh, int b0,
-                                                    const float *sSV, unsigned char *sMA, unsigned char *sMB) {
-    float hi[kMeanJ], lo[kMeanJ];
-    if (half == 0) {
-#pragma unroll
-        for (int i = 0; i < kMeanJ; ++i) split_bf16(sRS[i * kBlk + row], hi[i], lo[i]);
-    } else {
-        const float inv_sv = 1.0f / sSV[row];
-#pragma unroll
-        for (int i = 0; i < kMeanJ; ++i)
-            split_bf16(__fmul_rn(bf16_bits_to_f32(vmh[(b0 + i) * kD + row]), inv_sv), hi[i], lo[i]);
-    }
-    store_mean_row(half == 0 ? sMA : sMB, row, hi, lo, half == 0);
-}
 
 // O row part = (O_acc s_v + sum_t rs_t mu_t) / l for this thread's kCols
 // channels starting at col0: tO is the TMEM address of those accumulator
@@ -149,6 +129,40 @@ __device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, cons
     }
 }
 
+// A mean-restore MMA follows PV(b) for b = 19, 35, 51, ...: it adds the terms
+// of blocks b-19 .. b-4.  Their row sums are all visible to the thread that
+// stages them at block b (b is odd, so that thread takes the odd blocks): the
+// sum of an odd block j is written by the thread itself at block j+2 <= b-2,
+// the sum of an even block j <= b-5 by its partner at block j+2, before the
+// partner hands over the reference max at block j+4 <= b-1.
+constexpr int kMeanLag = 3;
+__host__ __device__ constexpr bool flush_after(int b) {
+    return b >= kMeanJ + kMeanLag && (b % kMeanJ) == kMeanLag;
+}
+
+// Operands of the mean-restore MMA for blocks b0 .. b0+15 (row / channel
+// `row`): A row = the row sums from their ring slots, each brought from the
+// reference max it was taken against to m; B row = mean / s_v.
+__device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
+                                            const uint16_t *sMeanGroup, const float *sSV, unsigned char *sMA,
+                                            unsigned char *sMB) {
+    float hi[kMeanJ], lo[kMeanJ];
+#pragma unroll
+    for (int i = 0; i < kMeanJ; ++i) {
+        const int slot = ((b0 + i) & (kRsSlots - 1)) * kBlk + row;
+        float rs = sRS[slot];
+        const float mt = sRSM[slot];
+        if (mt != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mt, m)));
+        split_bf16(rs, hi[i], lo[i]);
+    }
+    store_mean_row(sMA, row, hi, lo, true);
+    const float inv_sv = 1.0f / sSV[row];
+#pragma unroll
+    for (int i = 0; i < kMeanJ; ++i)
+        split_bf16(__fmul_rn(bf16_bits_to_f32(sMeanGroup[i * kD + row]), inv_sv), hi[i], lo[i]);
+    store_mean_row(sMB, row, hi, lo, false);
+}
+
 // Q tile row into TMEM (the A operand of QK): `row`'s 128 E4M3 codes as 32
 // columns at tq (this thread's lane).
 __device__ __forceinline__ void load_q_row(const uint8_t *q8row, uint32_t tq) {
@@ -178,6 +192,20 @@ inline bool make_tile_map(CUtensorMap *map, const void *base, uint64_t rows) {
     cuuint32_t estr[2] = {1, 1};
     return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 2-D byte matrix [rows][64] with 64 x 128 boxes and the 64-byte swizzle (the
+// NVFP4 V codes: one 128-channel block per box).
+inline bool make_tile_map_sw64(CUtensorMap *map, const void *base, uint64_t rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {64, rows};
+    cuuint64_t strides[1] = {64};
+    cuuint32_t box[2] = {64, 128};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

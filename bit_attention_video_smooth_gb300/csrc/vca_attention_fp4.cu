@@ -9,38 +9,50 @@
 // scale_vec::4X): P (A, E2M1 codes from TMEM) times V (B, E2M1 codes from
 // shared memory), each 16 keys of a row of either operand scaled by its E4M3
 // scale factor, which the MMA reads from TMEM; fp32 accumulation.  QK stays
-// E4M3 (kind::f8f6f4).  Layouts (measured on the hardware with a probe): P key k
-// at TMEM column k / 8, nibble k % 8; row m's four scales of a 64-key MMA in
-// lane m, column sfa + m / 32; B row n's, for the D rows of lane quarter q,
-// in lane 32 q + n % 32, column sfb + n / 32, so the V scales (and the ones'
+// E4M3 (kind::f8f6f4).  Layouts (measured on the hardware with probes): P key
+// k at TMEM column k / 8, nibble k % 8; row m's four scales of a 64-key MMA in
+// lane m, column sfa + m / 32; B row n's, for the D rows of lane quarter q, in
+// lane 32 q + n % 32, column sfb + n / 32, so the V scales (and the ones'
 // scales of the row-sum MMA) are present in all four lane quarters; the V
-// codes as a 128-byte-swizzled K-major tile whose 128-byte rows (one per
-// channel) carry the block's 128 keys in their first 64 bytes.
+// codes of a block as TMA writes them with the 64-byte swizzle (64-byte
+// channel rows, the block's 128 keys), a K-major B operand whose second
+// 64-key half starts 32 bytes into the rows.
 //
-// One CTA owns a 128-row query tile of one (batch, head).  Warp roles:
-//   warp 11      TMA producer: K tiles into a 3-stage ring
-//   warp 1       TMEM owner and MMA issuer (one thread); per key block j:
-//                  O += P_j V_j, E_{j&1} = P_j ones  (two block-scaled MMAs
-//                                 each, K = 64; the second gives P_j's row sums)
-//                  then the mean-restore MMA when due, then
-//                  S[j&1] = Q8 K8_{j+2}^T               (kind::f8f6f4)
-//   warps 0, 10  V layout: each block's packed codes (8 KB) into the swizzled
-//                tile, two channels per thread, and its scale factors into
-//                the 32-row matrices the MMA issuer copies into TMEM (one
-//                copy fills all four lane quarters); warp 0's lane 0
-//                bulk-copies block j+3's codes and scales into a 4-stage ring.
-//   warps 2-9    softmax, two threads per query row (column halves): running
-//                max with the lazy threshold, NVFP4 P of the row against it,
-//                P codes and scales into TMEM once PV(j-1) is done, row sum of
-//                block j-1 from its TMEM slot, O rescale, mean-restore
-//                operands, epilogue.
-// P has a single TMEM buffer, so P_j is written after PV(j-1) completes; the
-// softmax computes it while PV(j-1) runs.
+// One CTA owns a 128-row query tile of one (batch, head); the organisation is
+// the 8-bit kernel's.  Warp roles:
+//   warp 0     TMA producer: K tiles into a 3-stage ring
+//   warp 10    V producer: lane 0 loads each block's codes (TMA) and scales
+//              (bulk copy) into a 4-stage ring, three blocks ahead; the warp
+//              then lays the block's scales out as the two 32-row matrices the
+//              PV issuer copies into TMEM (one copy fills all four lane
+//              quarters) and marks the stage ready
+//   warp 11    QK issuer (one thread): S[b&1] = Q8 K8_b^T (kind::f8f6f4)
+//              once K(b) has landed and S(b-2) has been read
+//   warp 1     TMEM owner and PV issuer (one thread), per key block j:
+//                the V scales into TMEM (after PV(j-1): one buffer),
+//                O += P_j V_j, E_{j&1} = P_j ones   (two block-scaled MMAs
+//                                  each, K = 64; the second gives the row sums)
+//              and every 16 key blocks the bf16 mean-restore MMA
+//   warps 2-9  softmax, one thread per query row and key block: warps w and
+//              w+4 share a TMEM lane quarter and take the even and the odd key
+//              blocks.  Per block: the row max from the group maxima of the
+//              raw scores, the reference max handed over by the partner and
+//              updated with the lazy threshold, NVFP4 P of the row (codes and
+//              scales) into the P buffer of the block's parity, the row sum of
+//              block b-2 from its TMEM slot, O rescaled when the max moves,
+//              mean-restore operands when due, epilogue.
+// Barriers between the softmax and the MMA threads, per parity of b: s_full
+// (QK(b) committed), s_free (S(b) read), p_full (P(b) written), pv_done
+// (PV(b), its row sums and the mean MMA after it committed).
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), E0 [384,400),
-// E1 [400,416), P [416,432) (eight E2M1 codes per column), P scales
-// [432,440), V scales [440,456) (two buffers), ones' scales 456, Q [480,512).
-// Every wait is bounded; a wait that runs out raises a CTA-wide abort, the CTA
-// drains its copies and MMAs, frees TMEM and reports VCA_ERR_TIMEOUT.
+// E1 [400,416), P0 [416,432), P1 [432,448) (eight E2M1 codes per column),
+// P scales [448,456) and [456,464) per parity, V scales [464,472), the ones'
+// scales 472, Q [480,512).
+// Every wait on an mbarrier is bounded; a wait that runs out raises a CTA-wide
+// abort, the CTA drains its copies and MMAs, frees TMEM and reports
+// VCA_ERR_TIMEOUT.  Each named-barrier wait is matched by an arrival on every
+// path: a thread that gives up still hands on a reference max (NaN, which
+// makes its partner give up at its next block) before leaving the loop.
 #include "vca_attention_common.cuh"
 #include "vca_internal.h"
 
@@ -50,53 +62,48 @@ namespace {
 
 using namespace attn;
 
-constexpr int kKStages = 3;                  // K tiles in flight
-constexpr int kRawStages = 4;                // packed V blocks in flight
-constexpr int kVStages = 2;                  // swizzled V code tiles
-constexpr int kLayWarp0 = 0;                 // V layout; its lane 0 copies
-constexpr int kLayWarp1 = 2 + kSoftmaxWarps; // V layout
-constexpr int kLayWarps = 2;                 // two channels per thread
-constexpr int kKWarp = kLayWarp1 + 1;        // K producer
-// 12 warps: at most three per SM sub-partition, so up to 168 registers a thread
-constexpr int kThreads = 32 * (kKWarp + 1);
-constexpr int kRsCap = kMeanJ;               // buffered row sums per row
+constexpr int kKStages = 3;                  // K tiles in flight (released after their QK MMA)
+constexpr int kVStages = 4;                  // V blocks in flight (released after their PV MMA)
+constexpr int kVAhead = kVStages - 1;        // blocks the V loads run ahead of the layout
+constexpr int kVWarp = 2 + kSoftmaxWarps;    // the V producer
+constexpr int kQKWarp = kVWarp + 1;          // the QK issuer (the PV issuer is warp 1)
+constexpr int kThreads = 32 * (kQKWarp + 1);
 
 constexpr uint32_t kTileBytes = kBlk * kD;              // one 128 x 128 FP8 K tile
 constexpr uint32_t kCodeBytes = kD * kBlk / 2;          // a block's E2M1 codes, [ch][64 bytes]
 constexpr uint32_t kSfBytes = kD * kBlk / 16;           // a block's E4M3 scales, [ch][8]
-constexpr uint32_t kRawStageBytes = kCodeBytes + kSfBytes;
-constexpr uint32_t kVStageBytes = kD * 128;             // 128 channel rows of 128 bytes (codes in the first 64)
+constexpr uint32_t kSfbBytes = 32 * 16;                 // V scales of one 64-key MMA: 32 rows x 4 words
+constexpr uint32_t kVStageBytes = kCodeBytes + kSfBytes + 2 * kSfbBytes;   // [codes | scales | laid-out scales]
 constexpr uint32_t kOnesRows = 16;
 constexpr uint32_t kOnesBytes = kOnesRows * 128;        // 16 rows of E2M1 1.0: the row-sum MMA's B
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256, kTmemE0 = 384, kTmemE1 = 400, kTmemP = 416, kTmemSFA = 432, kTmemSFB = 440,
-                   kTmemSF1 = 456, kTmemQ = 480;
+constexpr uint32_t kTmemO = 256, kTmemE0 = 384, kTmemP0 = 416, kTmemSFA0 = 448, kTmemSFB = 464, kTmemSF1 = 472,
+                   kTmemQ = 480;
 
+// shared-memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t kOffK = 0;
 constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
 constexpr uint32_t kOffOnes = kOffV + kVStages * kVStageBytes;
-constexpr uint32_t kSfbBytes = 32 * 16;                  // V scales of one MMA: 32 rows x 4 words
-constexpr uint32_t kOffSfb = kOffOnes + kOnesBytes;        // [kVStages][2][kSfbBytes]
-constexpr uint32_t kOffRaw = kOffSfb + kVStages * 2 * kSfbBytes;
-constexpr uint32_t kOffMA = (kOffRaw + kRawStages * kRawStageBytes + 1023) & ~1023u;
+constexpr uint32_t kOffMA = kOffOnes + kOnesBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
-constexpr uint32_t kOffRS = kOffMB + kTileBytes;            // fp32 [kRsCap][128] buffered row sums
-constexpr uint32_t kOffSV = kOffRS + kRsCap * kBlk * 4;     // fp32 [128]: g for every channel
-constexpr uint32_t kOffPM = kOffSV + kBlk * 4;              // fp32 [2][kParts][128] part-row maxima
-constexpr uint32_t kOffL = kOffPM + 2 * kParts * kBlk * 4;  // fp32 [128] final row sums
-constexpr uint32_t kOffLg = kOffL + kBlk * 4;               // fp32 [128]: -log2(dec(E4M3 code)), -inf for code 0
+constexpr uint32_t kMeanGroupBytes = kMeanJ * kD * 2;        // bf16 means of 16 key blocks
+constexpr uint32_t kOffMean = kOffMB + kTileBytes;           // bf16 [2][16][128]: group g in buffer g & 1
+constexpr uint32_t kOffRS = kOffMean + 2 * kMeanGroupBytes;  // fp32 [kRsSlots][128] row sums (block j in slot j % 32)
+constexpr uint32_t kOffRSM = kOffRS + kRsSlots * kBlk * 4;   // fp32 [kRsSlots][128] the max each sum is taken against
+constexpr uint32_t kOffSV = kOffRSM + kRsSlots * kBlk * 4;   // fp32 [128] g for every channel
+constexpr uint32_t kOffMX = kOffSV + kBlk * 4;               // fp32 [2][128] reference max handed over, per parity
+constexpr uint32_t kOffL = kOffMX + 2 * kBlk * 4;            // fp32 [128] l, [2][128] partial l, [2][128] their max
+constexpr uint32_t kOffLg = kOffL + 5 * kBlk * 4;            // fp32 [128]: -log2(dec(E4M3 code)), -inf for code 0
 constexpr uint32_t kOffBar = kOffLg + kBlk * 4;
-constexpr int kNumBars = 1 + 2 * kKStages + 2 + kVStages + 2 * kRawStages + 1 + 2 + 1;
+constexpr int kNumBars = 1 + 2 * kKStages + 3 * kVStages + 2 * 4 + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kOffV % 1024 == 0 && kVStageBytes % 1024 == 0 && kOffOnes % 1024 == 0 && kOffMA % 1024 == 0 &&
                   kOffMB % 1024 == 0,
               "swizzled operand tiles need 1024-byte alignment");
-static_assert(kRawStageBytes % 16 == 0 && kOffRaw % 16 == 0, "bulk copies need 16-byte alignment");
-static_assert(kOffSfb % 128 == 0, "scale-factor copies start on a 16-byte boundary");
+static_assert(kCodeBytes % 16 == 0 && kSfBytes % 16 == 0 && kSfbBytes % 16 == 0, "copies need 16-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kD % (kLayWarps * 32) == 0, "layout threads cover the channels evenly");
-static_assert(kTmemSF1 < kTmemQ && kTmemSFB + 2 * 8 <= kTmemSF1, "TMEM plan");
+static_assert(kTmemSF1 < kTmemQ && kTmemSFB + 8 <= kTmemSF1 && kTmemSFA0 + 16 <= kTmemSFB, "TMEM plan");
 
 // Instruction descriptor of the block-scaled FP4 MMA: A and B E2M1, UE4M3 scale
 // factors (one per 16 elements, scale_vec::4X), scale-factor IDs 0, K = 64.
@@ -134,11 +141,11 @@ __device__ __forceinline__ void tc_cp_rows_x4(uint32_t taddr, uint64_t sdesc) {
 }
 
 struct Bars {
-    uint64_t *q_full, *k_full, *k_empty, *s_ready, *v_full, *raw_full, *raw_empty, *p_full, *pv_done, *drain;
+    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_ready, *v_empty, *s_full, *s_free, *p_full, *pv_done, *drain;
 };
 
 struct Params {
-    const uint8_t *q8, *v_code, *v_sf;
+    const uint8_t *q8, *v_sf;
     const float *sq, *sk, *v_scale;
     const uint16_t *v_mean;
     uint16_t *O;
@@ -148,90 +155,98 @@ struct Params {
     uint64_t limit_ns;
 };
 
-// The mean-restore MMA for key blocks j-16 .. j-1 follows PV(j); the softmax
-// stages its operands in step j, once block j-1's row sums are read.
-__host__ __device__ constexpr bool flush_after(int j) { return j >= kMeanJ && (j % kMeanJ) == 0; }
-
-// Largest raw score of each group of 16 of the thread's kCols keys.
-__device__ __forceinline__ void group_max(const uint32_t (&S)[kCols], float (&gm)[kCols / 16]) {
+// Largest raw score of each group of 16 of the kCols scores in X, into
+// gm[kG0 .. kG0 + kCols / 16).
+template <int kG0>
+__device__ __forceinline__ void group_max(const uint32_t (&X)[kCols], float (&gm)[kBlk / 16]) {
 #pragma unroll
     for (int g = 0; g < kCols / 16; ++g) {
-        const uint32_t *s = S + 16 * g;
+        const uint32_t *s = X + 16 * g;
         const float a = max3(__uint_as_float(s[0]), __uint_as_float(s[1]), __uint_as_float(s[2]));
         const float b = max3(__uint_as_float(s[3]), __uint_as_float(s[4]), __uint_as_float(s[5]));
         const float c = max3(__uint_as_float(s[6]), __uint_as_float(s[7]), __uint_as_float(s[8]));
         const float d = max3(__uint_as_float(s[9]), __uint_as_float(s[10]), __uint_as_float(s[11]));
         const float e = max3(__uint_as_float(s[12]), __uint_as_float(s[13]), __uint_as_float(s[14]));
-        gm[g] = fmaxf(max3(a, b, c), max3(d, e, __uint_as_float(s[15])));
+        gm[kG0 + g] = fmaxf(max3(a, b, c), max3(d, e, __uint_as_float(s[15])));
     }
 }
 
-// NVFP4 P of this thread's kCols keys against the reference max m: per group
-// of 16 keys p = 2^(fma(S, c, -m)), scale sf = E4M3(amax16 / 6), code =
-// E2M1(p / dec(sf)); P gets the codes (key k of the thread's keys at word
-// k / 8, nibble k % 8), sfa the four scale bytes (group g in byte g).
-// With c > 0, S -> 2^(fma(S, c, -m)) does not decrease, so amax16 is 2 to
-// the power of the group's largest score term (gm, from group_max).  The
+// NVFP4 P of one group of 16 keys, X[kOff .. kOff + 15], against the reference
+// max m (negm = -m): p = 2^(fma(S, c, -m)), scale sf = E4M3(amax16 / 6), code =
+// E2M1(p / dec(sf)); the codes go to W[kW], W[kW + 1] (key k of the group at
+// word k / 8, nibble k % 8), the scale byte is returned.
+// With c > 0, S -> 2^(fma(S, c, -m)) does not decrease, so amax16 is 2 to the
+// power of the group's largest score term (gmax, from group_max).  The
 // quotient amax16 / 6 is corrected by one FMA step,
 // q = RN(a r), q' = RN(q + RN(a - 6q) r) with r = RN(1/6): equal to the IEEE
 // quotient for every a in [2^-120, 2^30] (checked exhaustively), and below
 // that both round to the E4M3 code 0.  p / dec(sf) is evaluated as
-// 2^(fma(S, c, lg(sf) - m)) with lg(sf) = -log2(dec(sf)) from a per-CTA
-// table of the 127 codes (sLg; -inf for code 0, whose group codes are 0):
-// one FMA and one exp per key, the same hardware-exp accuracy as p itself.
-__device__ __forceinline__ void nvfp4_p(const uint32_t (&S)[kCols], const float (&gm)[kCols / 16], float c, float m,
-                                        const float *sLg, uint32_t (&P)[kCols / 8], uint32_t &sfa) {
+// 2^(fma(S, c, lg(sf) - m)) with lg(sf) = -log2(dec(sf)) from a per-CTA table
+// of the 127 codes (sLg; -inf for code 0, whose group codes are 0): one FMA and
+// one exp per key, the same hardware-exp accuracy as p itself.
+template <int kOff, int kW>
+__device__ __forceinline__ uint32_t nvfp4_group(const uint32_t (&X)[kCols], float gmax, float c, float negm,
+                                                uint64_t cx2, const float *sLg, uint32_t (&W)[kBlk / 8]) {
     constexpr float kSixth = 1.0f / 6.0f;
-    const float negm = -m;
-    const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
-    sfa = 0u;
+    const float amax = ex2_approx(__fmaf_rn(gmax, c, negm));
+    const float q0 = __fmul_rn(amax, kSixth);
+    const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), kSixth, q0);
+    const uint32_t sf = e4m3x2(q1, 0.0f) & 0xFFu;
+    const float bias = __fadd_rn(sLg[sf], negm);
+    const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
 #pragma unroll
-    for (int g = 0; g < kCols / 16; ++g) {
-        const float amax = ex2_approx(__fmaf_rn(gm[g], c, negm));
-        const float q0 = __fmul_rn(amax, kSixth);
-        const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), kSixth, q0);
-        const uint32_t sf = e4m3x2(q1, 0.0f) & 0xFFu;
-        sfa |= sf << (8 * g);
-        const float bias = __fadd_rn(sLg[sf], negm);
-        const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
+    for (int w = 0; w < 2; ++w) {
+        float x[8];
 #pragma unroll
-        for (int w = 0; w < 2; ++w) {
-            float x[8];
-#pragma unroll
-            for (int q = 0; q < 8; q += 2) {
-                float t0, t1;
-                upk2(fma2(pk2(S[16 * g + 8 * w + q], S[16 * g + 8 * w + q + 1]), cx2, bx2), t0, t1);
-                x[q] = ex2_approx(t0);
-                x[q + 1] = ex2_approx(t1);
-            }
-            P[2 * g + w] = e2m1x8(x);
+        for (int q = 0; q < 8; q += 2) {
+            float t0, t1;
+            upk2(fma2(pk2(X[kOff + 8 * w + q], X[kOff + 8 * w + q + 1]), cx2, bx2), t0, t1);
+            x[q] = ex2_approx(t0);
+            x[q + 1] = ex2_approx(t1);
         }
+        W[kW + w] = e2m1x8(x);
     }
+    return sf;
+}
+
+// Two groups (32 keys, X[kOff .. kOff + 31], group maxima gm[kG], gm[kG + 1]):
+// their codes into W[kW .. kW + 3], their two scale bytes as the low 16 bits.
+template <int kOff, int kW, int kG>
+__device__ __forceinline__ uint32_t nvfp4_32(const uint32_t (&X)[kCols], const float (&gm)[kBlk / 16], float c,
+                                             float negm, uint64_t cx2, const float *sLg, uint32_t (&W)[kBlk / 8]) {
+    const uint32_t s0 = nvfp4_group<kOff, kW>(X, gm[kG], c, negm, cx2, sLg, W);
+    const uint32_t s1 = nvfp4_group<kOff + 16, kW + 2>(X, gm[kG + 1], c, negm, cx2, sLg, W);
+    return s0 | (s1 << 8);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attention_nvfp4_kernel(const __grid_constant__ CUtensorMap tmK, const Params p) {
+    attention_nvfp4_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           const Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     Bars B;
     B.q_full = bars;
-    B.k_full = B.q_full + 1;
+    B.k_full = bars + 1;
     B.k_empty = B.k_full + kKStages;
-    B.s_ready = B.k_empty + kKStages;
-    B.v_full = B.s_ready + 2;
-    B.raw_full = B.v_full + kVStages;
-    B.raw_empty = B.raw_full + kRawStages;
-    B.p_full = B.raw_empty + kRawStages;
-    B.pv_done = B.p_full + 1;
-    B.drain = B.pv_done + 2;
+    B.v_full = B.k_empty + kKStages;
+    B.v_ready = B.v_full + kVStages;
+    B.v_empty = B.v_ready + kVStages;
+    B.s_full = B.v_empty + kVStages;
+    B.s_free = B.s_full + 2;
+    B.p_full = B.s_free + 2;
+    B.pv_done = B.p_full + 2;
+    B.drain = B.pv_done + 2;   // [0]: QK thread, [1]: PV thread
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_flag = reinterpret_cast<int *>(smem + kOffMisc + 4);
     float *sRS = reinterpret_cast<float *>(smem + kOffRS);
+    float *sRSM = reinterpret_cast<float *>(smem + kOffRSM);
     float *sSV = reinterpret_cast<float *>(smem + kOffSV);
-    float *sPM = reinterpret_cast<float *>(smem + kOffPM);
+    float *sMX = reinterpret_cast<float *>(smem + kOffMX);
     float *sL = reinterpret_cast<float *>(smem + kOffL);
+    float *sLp = sL + kBlk;        // [2][128] partial row sums, per parity
+    float *sMp = sL + 3 * kBlk;    // [2][128] the reference max they are taken against
     float *sLg = reinterpret_cast<float *>(smem + kOffLg);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -244,17 +259,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(B.k_full + s, 1);
             mbar_init(B.k_empty + s, 1);
         }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(B.v_full + s, 1);
+            mbar_init(B.v_ready + s, 1);
+            mbar_init(B.v_empty + s, 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(B.s_ready + i, 1);
+            mbar_init(B.s_full + i, 1);
+            mbar_init(B.s_free + i, kSoftmaxWarps / 2);
+            mbar_init(B.p_full + i, kSoftmaxWarps / 2);
             mbar_init(B.pv_done + i, 1);
+            mbar_init(B.drain + i, 1);
         }
-        for (int i = 0; i < kVStages; ++i) mbar_init(B.v_full + i, kLayWarps);
-        for (int s = 0; s < kRawStages; ++s) {
-            mbar_init(B.raw_full + s, 1);
-            mbar_init(B.raw_empty + s, kLayWarps);
-        }
-        mbar_init(B.p_full, kSoftmaxWarps);
-        mbar_init(B.drain, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -265,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp >= 2 && warp < 6) {
         const int t = threadIdx.x - 64;
         sSV[t] = p.v_scale[bh];
-        // scale tables for the E4M3 codes (127 = NaN is never produced)
+        // lg of the E4M3 codes (127 = NaN is never produced)
         sLg[t] = (t == 0 || t == 127) ? __int_as_float(0xff800000) : -log2f(e4m3_to_f32(static_cast<uint32_t>(t)));
         // the row-sum MMA's B: 16 rows of E2M1 1.0 (every nibble 2)
         const uint4 ones = make_uint4(0x22222222u, 0x22222222u, 0x22222222u, 0x22222222u);
@@ -277,8 +293,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == kKWarp) {
+    if (warp == 0) {
         // ------------------------------------------------------------ K producer
+        // a stage is refilled as soon as the QK MMA that read it has finished
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
             int armed[kKStages];
@@ -290,286 +307,352 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tma_load_2d(smem + kOffK + s * kTileBytes, &tmK, B.k_full + s, 0, bh * N + b * kBlk);
                 armed[s] = use + 1;
             }
+            // every copy this thread issued has landed before the CTA can exit
             for (int s = 0; s < kKStages; ++s)
                 if (armed[s] > 0) drain_wait(B.k_full + s, (armed[s] - 1) & 1, p.limit_ns);
         }
-    } else if (warp == kLayWarp0 || warp == kLayWarp1) {
-        // ------------------------------------------------------------ V layout
-        // Per channel ch: the 64 bytes of its 128 E2M1 codes (token 2i in the
-        // low nibble of byte i) as the first four 16-byte chunks of row ch of
-        // the swizzled tile.  The block's V scales are staged for the MMA
-        // issuer's copy into TMEM: for keys 64h.. (MMA h), row r of matrix
-        // (v, h) holds the four scales of channels r, r + 32, r + 64, r + 96
-        // (the MMA reads channel n's from lane n % 32 of the D row's lane
-        // quarter, column n / 32).
-        const bool lanes0 = warp == kLayWarp0;
-        const int t0 = (lanes0 ? 0 : 32) + lane;
-        const bool copier = (lanes0 && lane == 0);
-        int armed[kRawStages];
-        for (int s = 0; s < kRawStages; ++s) armed[s] = 0;
-        // block b's codes and scales into raw stage b % kRawStages, which the
-        // layout of block b - kRawStages (both warps) has released
-        auto copy_block = [&](int b) -> bool {
-            const int s = b % kRawStages, use = b / kRawStages;
-            if (use > 0 && !mbar_wait(B.raw_empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) return false;
+    } else if (warp == kVWarp) {
+        // ------------------------------------------------------------ V producer
+        // Lane 0 loads block b (codes by TMA with the 64-byte swizzle, scales,
+        // and with V(16 g) the bf16 means of group g into buffer g & 1) into
+        // stage b % kVStages once PV(b - kVStages) has released it.  The warp
+        // lays out block j's scales: row r of matrix h holds the scale words
+        // (keys 64h ..) of channels r, r + 32, r + 64, r + 96, the order in
+        // which the MMA reads B's scales from a lane quarter's columns.  The
+        // means group g - 2 that a buffer held was staged at block 16 g - 13,
+        // before PV(16 g - 4) completed, which the load of V(16 g) waited for.
+        int armed[kVStages];
+        for (int s = 0; s < kVStages; ++s) armed[s] = 0;
+        auto issue = [&](int b) -> bool {
+            const int s = b % kVStages, use = b / kVStages;
+            if (use > 0 && !mbar_wait(B.v_empty + s, (use - 1) & 1, abort_flag, p.limit_ns)) return false;
+            unsigned char *st = smem + kOffV + s * kVStageBytes;
             const int64_t blk = static_cast<int64_t>(bh) * nb + b;
-            unsigned char *dst = smem + kOffRaw + s * kRawStageBytes;
-            mbar_expect_tx(B.raw_full + s, kRawStageBytes);
-            bulk_load(dst, p.v_code + blk * kCodeBytes, kCodeBytes, B.raw_full + s);
-            bulk_load(dst + kCodeBytes, p.v_sf + blk * kSfBytes, kSfBytes, B.raw_full + s);
+            const bool with_means = (b % kMeanJ) == 0;
+            const uint32_t mean_bytes =
+                with_means ? static_cast<uint32_t>(nb - b < kMeanJ ? nb - b : kMeanJ) * kD * 2 : 0u;
+            mbar_expect_tx(B.v_full + s, kCodeBytes + kSfBytes + mean_bytes);
+            tma_load_2d(st, &tmV, B.v_full + s, 0, static_cast<int>(blk * kD));
+            bulk_load(st + kCodeBytes, p.v_sf + blk * kSfBytes, kSfBytes, B.v_full + s);
+            if (with_means)
+                bulk_load(smem + kOffMean + ((b / kMeanJ) & 1) * kMeanGroupBytes, p.v_mean + blk * kD, mean_bytes,
+                          B.v_full + s);
             armed[s] = use + 1;
             return true;
         };
-        bool cok = true;
-        if (copier)
-            for (int b = 0; cok && b < kRawStages - 1 && b < nb; ++b) cok = copy_block(b);
-        for (int j = 0; j < nb; ++j) {
-            const int s = j % kRawStages, v = j & 1;
-            if (copier && cok && j + kRawStages - 1 < nb) cok = copy_block(j + kRawStages - 1);
-            bool ok = cok && mbar_wait(B.raw_full + s, (j / kRawStages) & 1, abort_flag, p.limit_ns);
-            // tile v and the V-scale buffer v were last read by PV(j-2)
-            if (ok && j >= 2) ok = mbar_wait(B.pv_done + (j & 1), ((j - 2) >> 1) & 1, abort_flag, p.limit_ns);
-            if (!__all_sync(0xffffffffu, ok)) break;
-            const unsigned char *raw = smem + kOffRaw + s * kRawStageBytes;
-            unsigned char *vs = smem + kOffV + v * kVStageBytes;
-#pragma unroll
-            for (int t = t0; t < kD; t += 32 * kLayWarps) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    *reinterpret_cast<uint4 *>(vs + sw128_offset(t, i)) =
-                        reinterpret_cast<const uint4 *>(raw + t * (kBlk / 2))[i];
-            }
-            {
-                const int h = t0 >> 5;   // thread t0 stages row lane of matrix (v, h)
-                const unsigned char *sf = raw + kCodeBytes + 4 * h;
-                uint4 w;
-                w.x = *reinterpret_cast<const uint32_t *>(sf + (lane + 0) * (kBlk / 16));
-                w.y = *reinterpret_cast<const uint32_t *>(sf + (lane + 32) * (kBlk / 16));
-                w.z = *reinterpret_cast<const uint32_t *>(sf + (lane + 64) * (kBlk / 16));
-                w.w = *reinterpret_cast<const uint32_t *>(sf + (lane + 96) * (kBlk / 16));
-                *reinterpret_cast<uint4 *>(smem + kOffSfb + (2 * v + h) * kSfbBytes + 16 * lane) = w;
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.raw_empty + s);
-            fence_proxy_async_smem();   // the tile is read by the tensor core
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.v_full + v);
-        }
-        // every copy this thread issued has landed before the CTA can exit
-        if (copier)
-            for (int s = 0; s < kRawStages; ++s)
-                if (armed[s] > 0) drain_wait(B.raw_full + s, (armed[s] - 1) & 1, p.limit_ns);
-    } else if (warp == 1) {
-        // ------------------------------------------------------------ MMA issuer
+        bool lok = true;   // lane 0: every load so far issued
         if (lane == 0) {
-            constexpr uint32_t idesc_qk = make_idesc(128, 128, 0, 0);    // E4M3 x E4M3
-            constexpr uint32_t idesc_pv = make_idesc_mxf4(128, 128);     // NVFP4 x NVFP4
-            constexpr uint32_t idesc_rs = make_idesc_mxf4(128, kOnesRows);
-            constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);  // BF16 x BF16
+            tma_prefetch_desc(&tmV);
+            for (int b = 0; lok && b < kVAhead && b < nb; ++b) lok = issue(b);
+        }
+        for (int j = 0; j < nb; ++j) {
+            const int s = j % kVStages;
+            const bool landed = (lane != 0 || lok) && mbar_wait(B.v_full + s, (j / kVStages) & 1, abort_flag, p.limit_ns);
+            if (!__all_sync(0xffffffffu, landed)) break;
+            unsigned char *st = smem + kOffV + s * kVStageBytes;
+            const unsigned char *sf = st + kCodeBytes;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint4 w;
+                w.x = *reinterpret_cast<const uint32_t *>(sf + (lane + 0) * (kBlk / 16) + 4 * h);
+                w.y = *reinterpret_cast<const uint32_t *>(sf + (lane + 32) * (kBlk / 16) + 4 * h);
+                w.z = *reinterpret_cast<const uint32_t *>(sf + (lane + 64) * (kBlk / 16) + 4 * h);
+                w.w = *reinterpret_cast<const uint32_t *>(sf + (lane + 96) * (kBlk / 16) + 4 * h);
+                *reinterpret_cast<uint4 *>(st + kCodeBytes + kSfBytes + h * kSfbBytes + 16 * lane) = w;
+            }
+            fence_proxy_async_smem();   // read by the scale copy into TMEM
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(B.v_ready + s);
+                if (lok && j + kVAhead < nb) lok = issue(j + kVAhead);
+            }
+        }
+        // every copy lane 0 issued has landed before the CTA can exit
+        if (lane == 0)
+            for (int s = 0; s < kVStages; ++s)
+                if (armed[s] > 0) drain_wait(B.v_full + s, (armed[s] - 1) & 1, p.limit_ns);
+    } else if (warp == kQKWarp) {
+        // ------------------------------------------------------------ QK issuer
+        // QK(b) into S[b & 1] once K(b) has landed and the softmax has read
+        // S(b-2) out of that buffer; commits for the K stage and for s_full.
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = make_idesc(128, 128, 0, 0);
             const uint32_t sbase = smem_u32(smem);
-            const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
-            const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
-            const uint32_t tO = tmem + kTmemO;
-            // QK(b) into S[b & 1]; S(b-2) was read before P(b-2) was released
-            auto issue_qk = [&](int b) -> bool {
-                const int s = b % kKStages;
-                if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) return false;
+            bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
+            for (int b = 0; ok && b < nb; ++b) {
+                const int s = b % kKStages, sb = b & 1;
+                if (b >= 2 && !mbar_wait_spin(B.s_free + sb, ((b - 2) >> 1) & 1, abort_flag, p.limit_ns)) break;
+                if (!mbar_wait(B.k_full + s, (b / kKStages) & 1, abort_flag, p.limit_ns)) break;
                 tc_fence_after();
                 const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kD / 32; ++kk)
-                    mma_f8f6f4_ts(tmem + (b & 1) * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
+                    mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
                 tc_commit(B.k_empty + s);
-                tc_commit(B.s_ready + (b & 1));
-                return true;
-            };
-            bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
-            for (int b = 0; ok && b < 2 && b < nb; ++b) ok = issue_qk(b);
-            for (int j = 0; ok && j < nb; ++j) {
-                if (!mbar_wait(B.v_full + (j & 1), (j >> 1) & 1, abort_flag, p.limit_ns)) break;
-                tc_fence_after();
-                // block j's V scales into every lane quarter (buffer j & 1 was
-                // last read by PV(j-2), which finished before tile j was laid out)
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    tc_cp_rows_x4(tmem + kTmemSFB + 8 * (j & 1) + 4 * h,
-                                  sdesc_rows16(sbase + kOffSfb + (2 * (j & 1) + h) * kSfbBytes));
-                if (!mbar_wait(B.p_full, j & 1, abort_flag, p.limit_ns)) break;
-                tc_fence_after();
-                // O += P V and E_{j&1} = P ones, keys 64h .. 64h+63 per MMA
-                // (A columns 8h.., B bytes 32h.. of every row, scales at +4h)
-                const uint64_t dv = sdesc_k_sw128(sbase + kOffV + (j & 1) * kVStageBytes);
-                const uint64_t d1 = sdesc_k_sw128(sbase + kOffOnes);
-                const uint32_t te = tmem + ((j & 1) ? kTmemE1 : kTmemE0);
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    mma_mxf4_ts(tO, tmem + kTmemP + 8 * h, dv + 2 * h, idesc_pv, tmem + kTmemSFA + 4 * h,
-                                tmem + kTmemSFB + 8 * (j & 1) + 4 * h, (j > 0 || h > 0) ? 1u : 0u);
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-                    mma_mxf4_ts(te, tmem + kTmemP + 8 * h, d1 + 2 * h, idesc_rs, tmem + kTmemSFA + 4 * h, tmem + kTmemSF1,
-                                h > 0 ? 1u : 0u);
-                if (flush_after(j)) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
-                }
-                tc_commit(B.pv_done + (j & 1));
-                if (j + 2 < nb) ok = issue_qk(j + 2);
+                tc_commit(B.s_full + sb);
             }
             tc_commit(B.drain);
             drain_wait(B.drain, 0, p.limit_ns);
         }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ PV issuer
+        // PV(j) once V(j) is laid out and P(j) is written: block j's V scales
+        // into TMEM (their one buffer was last read by PV(j-1), which this
+        // thread waits for: in the steady state long done), O += P V and the
+        // row sums E_{j&1} = P ones, two K = 64 halves each, the mean-restore
+        // MMA when due, then commits for the V stage and for pv_done.
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = make_idesc_mxf4(128, 128);
+            constexpr uint32_t idesc_rs = make_idesc_mxf4(128, kOnesRows);
+            constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
+            const uint32_t sbase = smem_u32(smem);
+            const uint64_t dma = sdesc_k_sw128(sbase + kOffMA);
+            const uint64_t dmb = sdesc_k_sw128(sbase + kOffMB);
+            const uint64_t d1 = sdesc_k_sw128(sbase + kOffOnes);
+            const uint32_t tO = tmem + kTmemO;
+            for (int j = 0; j < nb; ++j) {
+                const int s = j % kVStages, pb = j & 1;
+                if (!mbar_wait(B.v_ready + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
+                if (j >= 1 && !mbar_wait_spin(B.pv_done + (pb ^ 1), ((j - 1) >> 1) & 1, abort_flag, p.limit_ns)) break;
+                tc_fence_after();
+                const uint32_t vst = sbase + kOffV + s * kVStageBytes;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    tc_cp_rows_x4(tmem + kTmemSFB + 4 * h, sdesc_rows16(vst + kCodeBytes + kSfBytes + h * kSfbBytes));
+                if (!mbar_wait_spin(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
+                tc_fence_after();
+                const uint64_t dv = sdesc_k_sw64(vst);
+                const uint32_t tp = tmem + kTmemP0 + 16 * pb;
+                const uint32_t tsfa = tmem + kTmemSFA0 + 8 * pb;
+                const uint32_t te = tmem + kTmemE0 + 16 * pb;
+                // keys 64h .. 64h + 63: A columns 8h.., B bytes 32h.. of every row, scales at +4h
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    mma_mxf4_ts(tO, tp + 8 * h, dv + 2 * h, idesc_pv, tsfa + 4 * h, tmem + kTmemSFB + 4 * h,
+                                (j > 0 || h > 0) ? 1u : 0u);
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    mma_mxf4_ts(te, tp + 8 * h, d1 + 2 * h, idesc_rs, tsfa + 4 * h, tmem + kTmemSF1, h > 0 ? 1u : 0u);
+                if (flush_after(j)) {
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) mma_f16(tO, dma + 2 * kk, dmb + 2 * kk, idesc_bf16, 1u);
+                }
+                tc_commit(B.v_empty + s);
+                tc_commit(B.pv_done + pb);
+            }
+            tc_commit(B.drain + 1);
+            drain_wait(B.drain + 1, 0, p.limit_ns);
+        }
     } else {
         // ------------------------------------------------------------ softmax
         const int quarter = warp & 3;                              // TMEM lane quarter
-        const int half = (warp - 2) >> 2;                          // column half: keys kCols*half ..
+        const int par = (warp - 2) >> 2;                           // this warp's key blocks: par, par + 2, ...
         const int row = quarter * 32 + lane;                       // query row in the tile == TMEM lane
-        const uint32_t pair_bar = kBarPair0 + quarter;
-        const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
-        const uint32_t col0 = static_cast<uint32_t>(kCols) * half;
-        const uint32_t tO = tmem + lane_base + kTmemO + col0;
-        const uint32_t tP = tmem + lane_base + kTmemP + (kCols / 8) * half;       // this half's codes
-        // its scales: the MMA reads row m's from lane m, column base + m / 32
-        const uint32_t tSFA = tmem + lane_base + kTmemSFA + 4 * half + quarter;
+        const uint32_t bar_out = kBarHand0 + 2 * quarter + par;    // hands the reference max on
+        const uint32_t bar_in = kBarHand0 + 2 * quarter + (par ^ 1);
+        const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
         const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
         unsigned char *sMA = smem + kOffMA;
         unsigned char *sMB = smem + kOffMB;
         const float kNegInf = __int_as_float(0xff800000);
-        float m = kNegInf;    // reference max
-        float l = 0.0f;       // kept by the half-0 thread of the row
-        int rs_cnt = 0;
+        float m = kNegInf;   // reference max after this thread's latest block
+        float l = 0.0f;      // row sum of this thread's blocks, taken against m
         bool ok = true;
-        float sk_next = skh[0];
-        if (half == 0) {
+        if (par == 0) {
+            // Q tile into TMEM (the A operand of QK): this row's 128 codes, 32 columns
             load_q_row(p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD,
-                       tmem + lane_base + kTmemQ);
+                       tl + kTmemQ);
             // the row-sum MMA's B scales (E4M3 1.0), read in every lane quarter
-            asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tmem + lane_base + kTmemSF1),
-                         "r"(0x38383838u) : "memory");
+            asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tl + kTmemSF1), "r"(0x38383838u)
+                         : "memory");
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(B.q_full);
         }
-        for (int b = 0; b < nb; ++b) {
+        float sk_next = par < nb ? skh[par] : 0.0f;
+        for (int b = par; b < nb; b += 2) {
             const int sb = b & 1;
             const float sk_b = sk_next;
-            if (b + 1 < nb) sk_next = skh[b + 1];
             const float c = __fmul_rn(__fmul_rn(sqv, sk_b), p.scale_log2);
-            bool wok = mbar_wait(B.s_ready + sb, (b >> 1) & 1, abort_flag, p.limit_ns);
-            wok = __all_sync(0xffffffffu, wok) && ok;
-            uint32_t S[kCols];
-            float gm[kCols / 16];
+            const uint32_t tS = tl + sb * 128;
+            // the group maxima of S(b); X keeps keys 64..127
+            uint32_t X[kCols];
+            float gm[kBlk / 16];
             float pm = kNegInf;
+            const bool wok = ok && __all_sync(0xffffffffu, mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns));
             if (wok) {
                 tc_fence_after();
-                const uint32_t tS = tmem + lane_base + sb * 128 + col0;
-#pragma unroll
-                for (int i = 0; i < kCols / 32; ++i) VCA_TMEM_LD32(tS + 32 * i, (S + 32 * i));
+                VCA_TMEM_LD32(tS, X);
+                VCA_TMEM_LD32(tS + 32, (X + 32));
                 tmem_ld_wait();
-                group_max(S, gm);
-                pm = gm[0];
-#pragma unroll
-                for (int g = 1; g < kCols / 16; ++g) pm = fmaxf(pm, gm[g]);
-                sPM[(sb * kParts + half) * kBlk + row] = pm;
+                group_max<0>(X, gm);
+                VCA_TMEM_LD32(tS + 64, X);
+                VCA_TMEM_LD32(tS + 96, (X + 32));
+                tmem_ld_wait();
+                group_max<kCols / 16>(X, gm);
+                pm = max3(max3(gm[0], gm[1], gm[2]), max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
             }
-            ok = bar_and(wok, pair_bar, 32 * kParts);
-            if (!ok) break;
-            float smax = pm;
-#pragma unroll
-            for (int q = 1; q < kParts; ++q) smax = fmaxf(smax, sPM[(sb * kParts + ((half + q) % kParts)) * kBlk + row]);
-            const float bm = __fmul_rn(smax, c);
-            // lazy reference-max update: only when the block's max exceeds it by tau
-            float alpha = 1.0f;
-            if (bm > __fadd_rn(m, kLazyTau)) {
-                if (b > 0) alpha = ex2_approx(__fsub_rn(m, bm));
-                m = bm;
+            // reference max after block b-1 (from the partner), after block b
+            // (handed on); NaN marks a partner that gave up
+            float m_in = kNegInf;
+            if (b >= 1) {
+                bar_sync(bar_in, 64);
+                m_in = sMX[(sb ^ 1) * kBlk + row];
             }
-            uint32_t P[kCols / 8], sfa;
-            nvfp4_p(S, gm, c, m, sLg, P, sfa);
-            // PV(b-1) is done: the P buffer and O are free, block b-1's row sums
-            // are in their slot
-            if (b >= 1) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + ((b - 1) & 1), ((b - 1) >> 1) & 1, abort_flag,
-                                                                p.limit_ns));
+            const bool valid = wok && !(m_in != m_in);
+            const float bm = __fmul_rn(pm, c);
+            const bool moved = valid && bm > __fadd_rn(m_in, kLazyTau);
+            const float m_new = moved ? bm : m_in;
+            if (b + 1 < nb) {
+                sMX[sb * kBlk + row] = valid ? m_new : __int_as_float(0x7fc00000);
+                bar_arrive_release(bar_out, 64);
+            }
+            // the next block's key scale, loaded after the hand-over so that the
+            // fence before it never waits for this load
+            if (b + 2 < nb) sk_next = skh[b + 2];
+            if (!__all_sync(0xffffffffu, valid)) {
+                ok = false;
+                break;
+            }
+            // NVFP4 P of all 128 keys: keys 64..127 from X while keys 0..63 are
+            // reloaded behind them; sfa0 / sfa1 the scale bytes of keys 0..63 / 64..127
+            const float negm = -m_new;
+            const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
+            uint32_t W[kBlk / 8];
+            uint32_t sfa1 = nvfp4_32<0, 8, 4>(X, gm, c, negm, cx2, sLg, W);
+            VCA_TMEM_LD32(tS, X);
+            sfa1 |= nvfp4_32<32, 12, 6>(X, gm, c, negm, cx2, sLg, W) << 16;
+            VCA_TMEM_LD32(tS + 32, (X + 32));
+            tmem_ld_wait();
+            // S(b) is read: QK(b+2) may overwrite the buffer
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(B.s_free + sb);
+            uint32_t sfa0 = nvfp4_32<0, 0, 0>(X, gm, c, negm, cx2, sLg, W);
+            sfa0 |= nvfp4_32<32, 4, 2>(X, gm, c, negm, cx2, sLg, W) << 16;
+            // P buffer b&1 and row-sum slot b&1 are free once PV(b-2) completed
+            if (b >= 2) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + sb, ((b - 2) >> 1) & 1, abort_flag, p.limit_ns));
             if (ok) {
                 tc_fence_after();
-                if (half == 0 && b >= 1) {
-                    // read block b-1's sums (taken against the max before this
-                    // block's update); PV(b)'s row-sum MMA overwrites this
-                    // block's slot
-                    const uint32_t te_prev = tmem + lane_base + (sb ? kTmemE0 : kTmemE1);
-                    uint32_t rs_raw;
-                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te_prev));
+                // block b-2's row sum from the slot of this parity, then P(b):
+                // the codes, and the row's scales in lane `row`, column
+                // sfa + 4h + quarter (PV(b)'s row-sum MMA rewrites the slot)
+                const uint32_t te = tl + kTmemE0 + 16 * sb;
+                uint32_t rs_raw = 0;
+                if (b >= 2) {
+                    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
                     tmem_ld_wait();
+                }
+                VCA_TMEM_ST16(tl + kTmemP0 + 16 * sb, W);
+                const uint32_t tsfa = tl + kTmemSFA0 + 8 * sb + quarter;
+                asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tsfa), "r"(sfa0) : "memory");
+                asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tsfa + 4), "r"(sfa1) : "memory");
+                if (b >= 2) {
+                    // block b-2's sum, taken against m (this thread's max after b-2)
                     const float rs = __uint_as_float(rs_raw);
+                    const int slot = ((b - 2) & (kRsSlots - 1)) * kBlk + row;
+                    sRS[slot] = rs;
+                    sRSM[slot] = m;
                     l = __fadd_rn(l, rs);
-                    sRS[rs_cnt * kBlk + row] = rs;
+                    if (m != m_new) l = __fmul_rn(l, ex2_approx(__fsub_rn(m, m_new)));
                 }
-                if (b >= 1) ++rs_cnt;
+                // the reference max moved at block b: O (after PV(b-1)) from m_in to m_new
+                const float alpha = (moved && b > 0) ? ex2_approx(__fsub_rn(m_in, m_new)) : 1.0f;
                 if (__any_sync(0xffffffffu, alpha != 1.0f)) {
-                    if (half == 0 && alpha != 1.0f) {
-                        l = __fmul_rn(l, alpha);
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(B.pv_done + (sb ^ 1), ((b - 1) >> 1) & 1, abort_flag, p.limit_ns));
+                    if (ok) {
+                        tc_fence_after();
 #pragma unroll 1
-                        for (int i = 0; i < rs_cnt; ++i) sRS[i * kBlk + row] = __fmul_rn(sRS[i * kBlk + row], alpha);
-                    }
-#pragma unroll 1
-                    for (int i = 0; i < kCols / 32; ++i) {
-                        uint32_t o[32];
-                        VCA_TMEM_LD32(tO + 32 * i, o);
-                        tmem_ld_wait();
+                        for (int i = 0; i < kD / 32; ++i) {
+                            uint32_t o[32];
+                            VCA_TMEM_LD32(tl + kTmemO + 32 * i, o);
+                            tmem_ld_wait();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
-                        VCA_TMEM_ST32(tO + 32 * i, o);
+                            for (int e = 0; e < 32; ++e)
+                                o[e] = __float_as_uint(__fmul_rn(__uint_as_float(o[e]), alpha));
+                            VCA_TMEM_ST32(tl + kTmemO + 32 * i, o);
+                        }
                     }
                 }
-                if (flush_after(b)) {
-                    // row sums of blocks b-16 .. b-1 (all at the current max)
-                    stage_mean_operands(half, row, sRS, vmh, b - kMeanJ, sSV, sMA, sMB);
-                    rs_cnt = 0;
-                    fence_proxy_async_smem();   // the mean operands are read by the tensor core
+                if (ok && flush_after(b)) {
+                    // mean-restore operands of blocks b-19 .. b-4 (the MMA follows PV(b))
+                    // the group's means landed with V(b0), before PV(b0) could run
+                    const int b0 = b - kMeanJ - kMeanLag;
+                    stage_means(row, sRS, sRSM, m_new, b0,
+                                reinterpret_cast<const uint16_t *>(smem + kOffMean) + ((b0 / kMeanJ) & 1) * (kMeanJ * kD),
+                                sSV, sMA, sMB);
+                    fence_proxy_async_smem();   // read by the tensor core
                 }
-                VCA_TMEM_ST8(tP, P);
-                asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tSFA), "r"(sfa) : "memory");
-                tmem_st_wait();
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(B.p_full);
+                if (ok) {
+                    tmem_st_wait();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(B.p_full + sb);
+                }
             }
+            m = m_new;
         }
         // ------------------------------------------------------------ epilogue
-        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + ((nb - 1) & 1), ((nb - 1) >> 1) & 1, abort_flag,
-                                                        p.limit_ns));
+        // this thread's last block lb: once PV(lb) has completed, its row sum
+        // is in the slot of this parity.  The wait is on this parity's barrier,
+        // whose previous phase (PV(lb-2)) this thread has seen complete.
+        const int lb = (((nb - 1) & 1) == par) ? nb - 1 : nb - 2;
+        if (ok && lb >= 0)
+            ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + par, (lb >> 1) & 1, abort_flag, p.limit_ns));
+        if (ok && lb >= 0) {
+            tc_fence_after();
+            uint32_t r = 0;
+            asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(tl + kTmemE0 + 16 * par));
+            tmem_ld_wait();
+            const float rs = __uint_as_float(r);
+            const int slot = (lb & (kRsSlots - 1)) * kBlk + row;
+            sRS[slot] = rs;
+            sRSM[slot] = m;
+            l = __fadd_rn(l, rs);
+        }
+        sLp[par * kBlk + row] = l;
+        sMp[par * kBlk + row] = lb >= 0 ? m : kNegInf;
         // every softmax warp arrives here, whether it finished or gave up; the
-        // epilogue (and its barriers) runs only if all of them finished
+        // epilogue (and its barriers) runs only if all of them finished.
+        // PV(nb-1), and with it every MMA, has completed once the threads of
+        // its parity have passed their wait above
         ok = bar_and(ok, kBarSoftmax, 32 * kSoftmaxWarps);
         if (ok) {
             tc_fence_after();
-            if (half == 0) {
-                // the last block's row sums, taken against m itself
-                uint32_t r1;
-                asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];"
-                             : "=r"(r1)
-                             : "r"(tmem + lane_base + (((nb - 1) & 1) ? kTmemE1 : kTmemE0)));
-                tmem_ld_wait();
-                const float rs = __uint_as_float(r1);
-                l = __fadd_rn(l, rs);
-                sRS[rs_cnt * kBlk + row] = rs;
-                sL[row] = l;
+            // the blocks after the last mean MMA's range
+            const int bf = nb - 1 >= kMeanJ + kMeanLag ? kMeanLag + kMeanJ * ((nb - 1 - kMeanLag) / kMeanJ) : -1;
+            const int tail0 = bf >= 0 ? bf - kMeanLag : 0;
+            const int rs_cnt = nb - tail0;
+            const float mf = sMp[((nb - 1) & 1) * kBlk + row];   // the final reference max
+            if (par == 0) {
+                float lt = 0.0f;
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {
+                    const float mq = sMp[q * kBlk + row];
+                    if (mq != kNegInf)
+                        lt = __fadd_rn(lt, mq == mf ? sLp[q * kBlk + row]
+                                                    : __fmul_rn(sLp[q * kBlk + row], ex2_approx(__fsub_rn(mq, mf))));
+                }
+                sL[row] = lt;
+                for (int t = 0; t < rs_cnt; ++t) {
+                    const int slot = ((tail0 + t) & (kRsSlots - 1)) * kBlk + row;
+                    if (sRSM[slot] != mf) sRS[slot] = __fmul_rn(sRS[slot], ex2_approx(__fsub_rn(sRSM[slot], mf)));
+                }
             }
-            ++rs_cnt;
-            // the blocks since the last mean MMA: stage their means (fp32) in the
-            // mean-B buffer, whose last reader (the final mean MMA) has finished
-            const int tail0 = nb - rs_cnt;
+            // the tail blocks' means (fp32) in the mean-B buffer, whose last
+            // reader (the final mean MMA) has finished
             float *sMu = reinterpret_cast<float *>(sMB);
-            bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             for (int i = threadIdx.x - 64; i < rs_cnt * kD; i += 32 * kSoftmaxWarps)
                 sMu[i] = bf16_bits_to_f32(vmh[(tail0 + i / kD) * kD + (i % kD)]);
             bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             const float inv_l = 1.0f / sL[row];
+            const int col0 = kCols * par;
             uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD + col0;
-            store_output(tO, sSV, sRS, sMu, rs_cnt, 0, row, static_cast<int>(col0), inv_l, orow);
+            store_output(tl + kTmemO + col0, sSV, sRS, sMu, rs_cnt, tail0, row, col0, inv_l, orow);
         }
     }
 
@@ -586,12 +669,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_attention_nvfp4(const AttentionArgs &a, cudaStream_t st) {
-    CUtensorMap mk;
+    CUtensorMap mk, mv;
     const uint64_t rows = static_cast<uint64_t>(a.BH) * a.N;
-    if (!make_tile_map(&mk, a.k8, rows)) return cudaErrorInvalidValue;
+    // K: [BH N][128] FP8 rows; V codes: [BH nb 128][64] bytes, one channel row per 128 keys
+    if (!make_tile_map(&mk, a.k8, rows) || !make_tile_map_sw64(&mv, a.v_res, rows)) return cudaErrorInvalidValue;
     Params p;
     p.q8 = a.q8;
-    p.v_code = a.v_res;
     p.v_sf = a.v_sf;
     p.sq = a.sq;
     p.sk = a.sk;
@@ -605,7 +688,7 @@ cudaError_t launch_attention_nvfp4(const AttentionArgs &a, cudaStream_t st) {
     const cudaError_t e =
         cudaFuncSetAttribute(attention_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attention_nvfp4_kernel<<<dim3(a.N / kBlk, a.BH), kThreads, kSmemBytes, st>>>(mk, p);
+    attention_nvfp4_kernel<<<dim3(a.N / kBlk, a.BH), kThreads, kSmemBytes, st>>>(mk, mv, p);
     return cudaGetLastError();
 }
 

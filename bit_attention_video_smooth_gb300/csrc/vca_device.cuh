@@ -259,6 +259,20 @@ __device__ __forceinline__ uint64_t sdesc_k_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory matrix descriptor for a K-major operand with the 64-byte
+// swizzle, as a TMA load with CU_TENSOR_MAP_SWIZZLE_64B writes it: rows of 64
+// bytes, 8-row atoms of 512 bytes one after another (the tile 512-byte
+// aligned).  A K step inside the row is a start-address step (16-byte units).
+__device__ __forceinline__ uint64_t sdesc_k_sw64(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address
+    d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused here)
+    d |= static_cast<uint64_t>(512 >> 4) << 32;             // stride byte offset: next 8-row atom
+    d |= static_cast<uint64_t>(1) << 46;                    // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(4) << 61;                    // 64-byte swizzle
+    return d;
+}
+
 // Shared-memory matrix descriptor for an MN-major 16-bit operand with the
 // 128-byte swizzle: rows are K indices, each row holds 64 consecutive M (or N)
 // elements (128 bytes), 8-row atoms of 1024 bytes follow each other along K

@@ -1,10 +1,11 @@
 """The attention kernels' TMEM column plans and shared-memory layouts, read
 from their sources and checked on the CPU.
 
-Both kernels hold S0, S1, two row-sum slots E0/E1 around the accumulator O, P
-and Q in the 512 TMEM columns of one CTA.  The PV MMA of an even block writes
-N = 144 columns [E0 | O] and of an odd block [O | E1], so those pairs must be
-contiguous; nothing may overlap.  Shared-memory tiles read by the tensor core
+Both kernels hold S0, S1, the accumulator O, two row-sum slots E0/E1, two P
+buffers and Q in the 512 TMEM columns of one CTA (the 4-bit kernel also the
+scale factors of its block-scaled MMAs).  The 8-bit kernel's PV MMA of an even
+block writes N = 144 columns [E0 | O] and of an odd block [O | E1], so those
+pairs must be contiguous; nothing may overlap.  Shared-memory tiles read by the tensor core
 with the 128-byte swizzle start on 1024-byte boundaries, mbarriers on 8-byte
 ones, and the whole layout fits the 227 KB a CTA may use.
 """
@@ -87,41 +88,47 @@ def test_e4m3_shared_memory_layout(e4m3):
 
 
 def test_nvfp4_tmem_plan(nvfp4):
-    """The 4-bit kernel's columns: P as E2M1 codes (128 keys at eight per
-    column), its scales (two MMAs x four lane-quarter columns), V's scales
-    (two buffers x two MMAs x four columns of lanes 0-31) and the ones rows'
-    scale column, none overlapping S, O, the row-sum slots or Q."""
+    """The 4-bit kernel's columns: two P buffers as E2M1 codes (128 keys at
+    eight per column), their scales (per parity two MMAs x four lane-quarter
+    columns), one V-scale buffer (two MMAs x four columns, filled in every lane
+    quarter) and the ones rows' scale column, none overlapping S, O, the
+    row-sum slots or Q."""
     c = nvfp4
     cols = {"S0": (0, 128), "S1": (128, 256), "O": (c["kTmemO"], c["kTmemO"] + 128),
-            "E0": (c["kTmemE0"], c["kTmemE0"] + 16), "E1": (c["kTmemE1"], c["kTmemE1"] + 16),
-            "P": (c["kTmemP"], c["kTmemP"] + 128 // 8), "SFA": (c["kTmemSFA"], c["kTmemSFA"] + 2 * 4),
-            "SFB": (c["kTmemSFB"], c["kTmemSFB"] + 2 * 2 * 4), "SF1": (c["kTmemSF1"], c["kTmemSF1"] + 1),
+            "E0": (c["kTmemE0"], c["kTmemE0"] + 16), "E1": (c["kTmemE0"] + 16, c["kTmemE0"] + 32),
+            "P0": (c["kTmemP0"], c["kTmemP0"] + 128 // 8), "P1": (c["kTmemP0"] + 16, c["kTmemP0"] + 32),
+            "SFA0": (c["kTmemSFA0"], c["kTmemSFA0"] + 2 * 4), "SFA1": (c["kTmemSFA0"] + 8, c["kTmemSFA0"] + 16),
+            "SFB": (c["kTmemSFB"], c["kTmemSFB"] + 2 * 4), "SF1": (c["kTmemSF1"], c["kTmemSF1"] + 1),
             "Q": (c["kTmemQ"], c["kTmemQ"] + 32)}
     _disjoint(cols, c["kTmemCols"])
     # the row-sum MMA writes N = 16 columns into a slot of 16
     assert c["kOnesRows"] == 16
+    # 32 mbarriers' worth of roles: Q, the K ring, the V ring (landed, laid
+    # out, released), S / P / PV per parity and the two issuers' drains
+    assert c["kNumBars"] == 1 + 2 * c["kKStages"] + 3 * c["kVStages"] + 2 * 5
 
 
 def test_nvfp4_shared_memory_layout(nvfp4):
     c = nvfp4
     assert c["kThreads"] == 384
-    assert c["kVStageBytes"] == 128 * 128                                      # a channel row of 128 bytes
+    # a V stage: the block's codes as TMA writes them with the 64-byte swizzle
+    # (128 channel rows of 64 bytes, 512-byte atoms), its raw scales and the two
+    # 32-row x 16-byte matrices the PV issuer copies into TMEM
+    assert c["kVStageBytes"] == 128 * 64 + 1024 + 2 * 512
     for s in range(c["kVStages"]):
-        assert (c["kOffV"] + s * c["kVStageBytes"]) % 1024 == 0                # swizzled B tiles
+        st = c["kOffV"] + s * c["kVStageBytes"]
+        assert st % 1024 == 0                                                  # swizzle atoms
+        assert (st + c["kCodeBytes"]) % 16 == 0                                # bulk-copy destination
+        assert (st + c["kCodeBytes"] + c["kSfBytes"]) % 16 == 0                # scale-copy source
     assert c["kOffOnes"] % 1024 == 0 and c["kOnesBytes"] == 16 * 128
     assert c["kOffMA"] % 1024 == 0 and c["kOffMB"] % 1024 == 0
-    # the V-scale matrices the MMA issuer copies into TMEM: 32 rows of 16 bytes,
-    # one per stage and 64-key half, on 16-byte boundaries
-    assert c["kSfbBytes"] == 32 * 16 and c["kOffSfb"] % 16 == 0
-    assert c["kOffSfb"] >= c["kOffOnes"] + c["kOnesBytes"]
-    assert c["kOffSfb"] + c["kVStages"] * 2 * c["kSfbBytes"] <= c["kOffRaw"]
-    for s in range(c["kRawStages"]):
-        assert (c["kOffRaw"] + s * c["kRawStageBytes"]) % 16 == 0                 # bulk copy destinations
     assert c["kOffBar"] % 8 == 0 and c["kSmemBytes"] <= 232448
-    order = ["kOffK", "kOffV", "kOffOnes", "kOffSfb", "kOffRaw", "kOffMA", "kOffMB", "kOffRS", "kOffSV", "kOffPM", "kOffL",
-             "kOffLg", "kOffBar", "kOffMisc"]
+    order = ["kOffK", "kOffV", "kOffOnes", "kOffMA", "kOffMB", "kOffMean", "kOffRS", "kOffRSM", "kOffSV", "kOffMX",
+             "kOffL", "kOffLg", "kOffBar", "kOffMisc"]
     offs = [c[k] for k in order]
     assert offs == sorted(offs)
+    # the V loads run ahead by all stages but the one being laid out
+    assert c["kVAhead"] == c["kVStages"] - 1
 
 
 def test_the_evaluator_reads_the_sources(e4m3, nvfp4):

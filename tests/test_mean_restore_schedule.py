@@ -1,5 +1,5 @@
-"""A model of the E4M3 attention kernel's mean-restore schedule, checked on the
-CPU for every block count up to 600.
+"""A model of the attention kernels' mean-restore schedule (the 8-bit and the
+4-bit kernel share it), checked on the CPU for every block count up to 600.
 
 Per query row the kernel keeps each key block's row sum in a ring of kRsSlots
 shared-memory slots (block j in slot j % kRsSlots): the thread of the block's
@@ -32,17 +32,20 @@ def _const(text, name):
     return int(m.group(1))
 
 
-@pytest.fixture(scope="module")
-def K():
+@pytest.fixture(scope="module", params=["vca_attention.cu", "vca_attention_fp4.cu"])
+def K(request):
+    """The schedule as the shared header defines it, checked to be the one each
+    kernel (8-bit and 4-bit) follows."""
     common = open(os.path.join(CSRC, "vca_attention_common.cuh")).read()
-    kern = open(os.path.join(CSRC, "vca_attention.cu")).read()
-    # the rules the model restates, as the kernel writes them
-    assert "return b >= kMeanJ + kMeanLag && (b % kMeanJ) == kMeanLag;" in kern
+    kern = open(os.path.join(CSRC, request.param)).read()
+    # the rules the model restates, as the kernels write them
+    assert "return b >= kMeanJ + kMeanLag && (b % kMeanJ) == kMeanLag;" in common
     assert "const int bf = nb - 1 >= kMeanJ + kMeanLag ? kMeanLag + kMeanJ * ((nb - 1 - kMeanLag) / kMeanJ) : -1;" in kern
     assert "const int tail0 = bf >= 0 ? bf - kMeanLag : 0;" in kern
     assert "const int b0 = b - kMeanJ - kMeanLag;" in kern
     assert "stage_means(row, sRS, sRSM, m_new, b0," in kern
-    return {"J": _const(common, "kMeanJ"), "L": _const(kern, "kMeanLag"), "S": _const(common, "kRsSlots"),
+    assert "if (flush_after(j))" in kern and "if (ok && flush_after(b))" in kern
+    return {"J": _const(common, "kMeanJ"), "L": _const(common, "kMeanLag"), "S": _const(common, "kRsSlots"),
             "blk": 128, "d": 128, "tile_bytes": 128 * 128}
 
 
