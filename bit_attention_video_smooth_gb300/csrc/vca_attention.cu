@@ -370,14 +370,28 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool wok = ok && __all_sync(0xffffffffu, mbar_wait(B.s_full + sb, (b >> 1) & 1, abort_flag, p.limit_ns));
             if (wok) {
                 tc_fence_after();
-                VCA_TMEM_LD32(tS, X);
-                VCA_TMEM_LD32(tS + 32, (X + 32));
-                tmem_ld_wait();
-                pm = row_part_max(X);
-                VCA_TMEM_LD32(tS + 64, X);
-                VCA_TMEM_LD32(tS + 96, (X + 32));
-                tmem_ld_wait();
-                pm = fmaxf(pm, row_part_max(X));
+                if constexpr (kExpcast) {
+                    // the reducing loads return each 32 columns' max with the
+                    // data (in the exp-path build they cost more in spills
+                    // than the max instructions they save)
+                    float r0, r1, r2, r3;
+                    VCA_TMEM_LDMAX32(tS, X, r0);
+                    VCA_TMEM_LDMAX32(tS + 32, (X + 32), r1);
+                    tmem_ld_wait();
+                    VCA_TMEM_LDMAX32(tS + 64, X, r2);
+                    VCA_TMEM_LDMAX32(tS + 96, (X + 32), r3);
+                    tmem_ld_wait();
+                    pm = fmaxf(fmaxf(r0, r1), fmaxf(r2, r3));
+                } else {
+                    VCA_TMEM_LD32(tS, X);
+                    VCA_TMEM_LD32(tS + 32, (X + 32));
+                    tmem_ld_wait();
+                    pm = row_part_max(X);
+                    VCA_TMEM_LD32(tS + 64, X);
+                    VCA_TMEM_LD32(tS + 96, (X + 32));
+                    tmem_ld_wait();
+                    pm = fmaxf(pm, row_part_max(X));
+                }
             }
             // reference max after block b-1 (from the partner), after block b
             // (handed on); NaN marks a partner that gave up

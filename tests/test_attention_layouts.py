@@ -90,16 +90,16 @@ def test_e4m3_shared_memory_layout(e4m3):
 def test_nvfp4_tmem_plan(nvfp4):
     """The 4-bit kernel's columns: two P buffers as E2M1 codes (128 keys at
     eight per column), their scales (per parity two MMAs x four lane-quarter
-    columns), one V-scale buffer (two MMAs x four columns, filled in every lane
-    quarter) and the ones rows' scale column, none overlapping S, O, the
-    row-sum slots or Q."""
+    columns), two V-scale buffers (per parity two MMAs x four columns, filled
+    in every lane quarter) and the ones rows' scale column, none overlapping S,
+    O or the row-sum slots (Q is QK's A operand from shared memory here)."""
     c = nvfp4
     cols = {"S0": (0, 128), "S1": (128, 256), "O": (c["kTmemO"], c["kTmemO"] + 128),
             "E0": (c["kTmemE0"], c["kTmemE0"] + 16), "E1": (c["kTmemE0"] + 16, c["kTmemE0"] + 32),
             "P0": (c["kTmemP0"], c["kTmemP0"] + 128 // 8), "P1": (c["kTmemP0"] + 16, c["kTmemP0"] + 32),
             "SFA0": (c["kTmemSFA0"], c["kTmemSFA0"] + 2 * 4), "SFA1": (c["kTmemSFA0"] + 8, c["kTmemSFA0"] + 16),
-            "SFB": (c["kTmemSFB"], c["kTmemSFB"] + 2 * 4), "SF1": (c["kTmemSF1"], c["kTmemSF1"] + 1),
-            "Q": (c["kTmemQ"], c["kTmemQ"] + 32)}
+            "SFB0": (c["kTmemSFB"], c["kTmemSFB"] + 2 * 4), "SFB1": (c["kTmemSFB"] + 8, c["kTmemSFB"] + 16),
+            "SF1": (c["kTmemSF1"], c["kTmemSF1"] + 1)}
     _disjoint(cols, c["kTmemCols"])
     # the row-sum MMA writes N = 16 columns into a slot of 16
     assert c["kOnesRows"] == 16
@@ -123,8 +123,9 @@ def test_nvfp4_shared_memory_layout(nvfp4):
     assert c["kOffOnes"] % 1024 == 0 and c["kOnesBytes"] == 16 * 128
     assert c["kOffMA"] % 1024 == 0 and c["kOffMB"] % 1024 == 0
     assert c["kOffBar"] % 8 == 0 and c["kSmemBytes"] <= 232448
-    order = ["kOffK", "kOffV", "kOffOnes", "kOffMA", "kOffMB", "kOffMean", "kOffRS", "kOffRSM", "kOffSV", "kOffMX",
-             "kOffL", "kOffLg", "kOffBar", "kOffMisc"]
+    assert c["kOffQ"] % 1024 == 0 and c["kOffV"] >= c["kOffQ"] + 128 * 128   # the swizzled Q tile
+    order = ["kOffK", "kOffQ", "kOffV", "kOffOnes", "kOffMA", "kOffMB", "kOffMean", "kOffRS", "kOffRSM", "kOffSV",
+             "kOffMX", "kOffL", "kOffLg", "kOffBar", "kOffMisc"]
     offs = [c[k] for k in order]
     assert offs == sorted(offs)
     # the V loads run ahead by all stages but the one being laid out
