@@ -372,8 +372,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 if constexpr (kExpcast) {
                     // the reducing loads return each 32 columns' max with the
-                    // data (in the exp-path build they cost more in spills
-                    // than the max instructions they save)
+                    // data (the exp-path build takes them for columns 64..127
+                    // only: for both halves they cost it more in spills than
+                    // the max instructions they save)
                     float r0, r1, r2, r3;
                     VCA_TMEM_LDMAX32(tS, X, r0);
                     VCA_TMEM_LDMAX32(tS + 32, (X + 32), r1);
@@ -387,10 +388,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     VCA_TMEM_LD32(tS + 32, (X + 32));
                     tmem_ld_wait();
                     pm = row_part_max(X);
-                    VCA_TMEM_LD32(tS + 64, X);
-                    VCA_TMEM_LD32(tS + 96, (X + 32));
+                    float r2, r3;
+                    VCA_TMEM_LDMAX32(tS + 64, X, r2);
+                    VCA_TMEM_LDMAX32(tS + 96, (X + 32), r3);
                     tmem_ld_wait();
-                    pm = fmaxf(pm, row_part_max(X));
+                    pm = fmaxf(pm, fmaxf(r2, r3));
                 }
             }
             // reference max after block b-1 (from the partner), after block b
@@ -438,12 +440,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // block b-2's row sum from the slot of this parity, then P(b) and
                 // the cleared slot for PV(b) (PV(0) initialises E0)
                 const uint32_t te = tl + (sb == 0 ? kTmemE0 : kTmemE1);
+                // the exp-path build stores P before reading the slot, the
+                // ExpCast build after (each order measured faster for its build)
+                if constexpr (!kExpcast) VCA_TMEM_ST32(tp, W);
                 uint32_t rs_raw = 0;
                 if (b >= 2) {
                     asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(rs_raw) : "r"(te));
                     tmem_ld_wait();
                 }
-                VCA_TMEM_ST32(tp, W);
+                if constexpr (kExpcast) VCA_TMEM_ST32(tp, W);
                 if (b >= 1)
                     asm volatile(
                         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1,%1};"

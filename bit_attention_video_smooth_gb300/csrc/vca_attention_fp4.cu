@@ -491,10 +491,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 VCA_TMEM_LD32(tS + 32, (X + 32));
                 tmem_ld_wait();
                 group_max<0>(X, gm);
-                VCA_TMEM_LD32(tS + 64, X);
-                VCA_TMEM_LD32(tS + 96, (X + 32));
+                // keys 64..127 by reducing loads, which return each 16 keys' max
+                // with the data (for keys 0..63 as well they cost more in spills)
+                VCA_TMEM_LDMAX16(tS + 64, X, gm[4]);
+                VCA_TMEM_LDMAX16(tS + 80, (X + 16), gm[5]);
+                VCA_TMEM_LDMAX16(tS + 96, (X + 32), gm[6]);
+                VCA_TMEM_LDMAX16(tS + 112, (X + 48), gm[7]);
                 tmem_ld_wait();
-                group_max<kCols / 16>(X, gm);
                 pm = max3(max3(gm[0], gm[1], gm[2]), max3(gm[3], gm[4], gm[5]), fmaxf(gm[6], gm[7]));
             }
             // reference max after block b-1 (from the partner), after block b
