@@ -173,28 +173,50 @@ __device__ __forceinline__ void group_max(const uint32_t (&X)[kCols], float (&gm
     }
 }
 
-// NVFP4 P of one group of 16 keys, X[kOff .. kOff + 15], against the reference
-// max m (negm = -m): p = 2^(fma(S, c, -m)), scale sf = E4M3(amax16 / 6), code =
-// E2M1(p / dec(sf)); the codes go to W[kW], W[kW + 1] (key k of the group at
-// word k / 8, nibble k % 8), the scale byte is returned.
+// NVFP4 P of a row against the reference max m (negm = -m): per group of 16
+// keys p = 2^(fma(S, c, -m)), scale sf = E4M3(amax16 / 6), code =
+// E2M1(p / dec(sf)); P's codes go to W (key k at word k / 8, nibble k % 8),
+// the scale bytes to a word per 64 keys (group g in byte g).
 // With c > 0, S -> 2^(fma(S, c, -m)) does not decrease, so amax16 is 2 to the
-// power of the group's largest score term (gmax, from group_max).  The
-// quotient amax16 / 6 is corrected by one FMA step,
+// power of the group's largest score term (gm, from group_max or the reducing
+// loads).  The quotient amax16 / 6 is corrected by one FMA step,
 // q = RN(a r), q' = RN(q + RN(a - 6q) r) with r = RN(1/6): equal to the IEEE
 // quotient for every a in [2^-120, 2^30] (checked exhaustively), and below
 // that both round to the E4M3 code 0.  p / dec(sf) is evaluated as
 // 2^(fma(S, c, lg(sf) - m)) with lg(sf) = -log2(dec(sf)) from a per-CTA table
 // of the 127 codes (sLg; -inf for code 0, whose group codes are 0): one FMA and
 // one exp per key, the same hardware-exp accuracy as p itself.
-template <int kOff, int kW>
-__device__ __forceinline__ uint32_t nvfp4_group(const uint32_t (&X)[kCols], float gmax, float c, float negm,
-                                                uint64_t cx2, const float *sLg, uint32_t (&W)[kBlk / 8]) {
+//
+// Scales of the four groups kG .. kG + 3 (maxima gm[kG + i]): the scale word
+// (group i in byte i) is returned, bias[kB + i] = lg(sf_i) - m; two groups per
+// packed instruction and per E4M3 convert, each rounded as alone.
+template <int kG, int kB>
+__device__ __forceinline__ uint32_t nvfp4_scales4(const float (&gm)[kBlk / 16], float c, float negm, const float *sLg,
+                                                  float (&bias)[kBlk / 16]) {
     constexpr float kSixth = 1.0f / 6.0f;
-    const float amax = ex2_approx(__fmaf_rn(gmax, c, negm));
-    const float q0 = __fmul_rn(amax, kSixth);
-    const float q1 = __fmaf_rn(__fmaf_rn(-q0, 6.0f, amax), kSixth, q0);
-    const uint32_t sf = e4m3x2(q1, 0.0f) & 0xFFu;
-    const float bias = __fadd_rn(sLg[sf], negm);
+    float a[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) a[i] = ex2_approx(__fmaf_rn(gm[kG + i], c, negm));
+    const uint64_t r6 = pk2(__float_as_uint(kSixth), __float_as_uint(kSixth));
+    const uint64_t m6 = pk2(__float_as_uint(-6.0f), __float_as_uint(-6.0f));
+    float q[4];
+#pragma unroll
+    for (int i = 0; i < 4; i += 2) {
+        const uint64_t a2 = pk2(__float_as_uint(a[i]), __float_as_uint(a[i + 1]));
+        const uint64_t q0 = mul2(a2, r6);
+        upk2(fma2(fma2(q0, m6, a2), r6, q0), q[i], q[i + 1]);
+    }
+    const uint32_t sfa = (e4m3x2(q[0], q[1]) & 0xFFFFu) | (e4m3x2(q[2], q[3]) << 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bias[kB + i] = __fadd_rn(sLg[(sfa >> (8 * i)) & 0xFFu], negm);
+    return sfa;
+}
+
+// E2M1 codes of one group of 16 keys X[kOff .. kOff + 15] into W[kW], W[kW + 1]:
+// E2M1(2^(fma(S, c, bias))) with bias = lg(sf) - m.
+template <int kOff, int kW>
+__device__ __forceinline__ void nvfp4_codes16(const uint32_t (&X)[kCols], float bias, uint64_t cx2,
+                                              uint32_t (&W)[kBlk / 8]) {
     const uint64_t bx2 = pk2(__float_as_uint(bias), __float_as_uint(bias));
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
@@ -208,17 +230,6 @@ __device__ __forceinline__ uint32_t nvfp4_group(const uint32_t (&X)[kCols], floa
         }
         W[kW + w] = e2m1x8(x);
     }
-    return sf;
-}
-
-// Two groups (32 keys, X[kOff .. kOff + 31], group maxima gm[kG], gm[kG + 1]):
-// their codes into W[kW .. kW + 3], their two scale bytes as the low 16 bits.
-template <int kOff, int kW, int kG>
-__device__ __forceinline__ uint32_t nvfp4_32(const uint32_t (&X)[kCols], const float (&gm)[kBlk / 16], float c,
-                                             float negm, uint64_t cx2, const float *sLg, uint32_t (&W)[kBlk / 8]) {
-    const uint32_t s0 = nvfp4_group<kOff, kW>(X, gm[kG], c, negm, cx2, sLg, W);
-    const uint32_t s1 = nvfp4_group<kOff + 16, kW + 2>(X, gm[kG + 1], c, negm, cx2, sLg, W);
-    return s0 | (s1 << 8);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -527,17 +538,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float negm = -m_new;
             const uint64_t cx2 = pk2(__float_as_uint(c), __float_as_uint(c));
             uint32_t W[kBlk / 8];
-            uint32_t sfa1 = nvfp4_32<0, 8, 4>(X, gm, c, negm, cx2, sLg, W);
+            float bias[kBlk / 16];
+            const uint32_t sfa1 = nvfp4_scales4<4, 4>(gm, c, negm, sLg, bias);
+            nvfp4_codes16<0, 8>(X, bias[4], cx2, W);
+            nvfp4_codes16<16, 10>(X, bias[5], cx2, W);
             VCA_TMEM_LD32(tS, X);
-            sfa1 |= nvfp4_32<32, 12, 6>(X, gm, c, negm, cx2, sLg, W) << 16;
+            nvfp4_codes16<32, 12>(X, bias[6], cx2, W);
+            nvfp4_codes16<48, 14>(X, bias[7], cx2, W);
             VCA_TMEM_LD32(tS + 32, (X + 32));
             tmem_ld_wait();
             // S(b) is read: QK(b+2) may overwrite the buffer
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(B.s_free + sb);
-            uint32_t sfa0 = nvfp4_32<0, 0, 0>(X, gm, c, negm, cx2, sLg, W);
-            sfa0 |= nvfp4_32<32, 4, 2>(X, gm, c, negm, cx2, sLg, W) << 16;
+            const uint32_t sfa0 = nvfp4_scales4<0, 0>(gm, c, negm, sLg, bias);
+            nvfp4_codes16<0, 0>(X, bias[0], cx2, W);
+            nvfp4_codes16<16, 2>(X, bias[1], cx2, W);
+            nvfp4_codes16<32, 4>(X, bias[2], cx2, W);
+            nvfp4_codes16<48, 6>(X, bias[3], cx2, W);
             // P buffer b&1 and row-sum slot b&1 are free once PV(b-2) completed
             if (b >= 2) ok = __all_sync(0xffffffffu, mbar_wait(B.pv_done + sb, ((b - 2) >> 1) & 1, abort_flag, p.limit_ns));
             if (ok) {
