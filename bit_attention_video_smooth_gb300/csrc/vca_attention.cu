@@ -221,8 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, kTmemCols);
         tmem_relinquish();
     }
+    // the Q tile: warps 2-5 (the even-block softmax warps, one query row per
+    // thread) load their rows now and store them into TMEM once it is allocated
+    uint32_t qv[32];
     if (warp >= 2 && warp < 6) {
         const int t = threadIdx.x - 64;
+        load_q_regs(p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + (warp & 3) * 32 + lane) * kD,
+                    qv);
         sSV[t] = p.v_scale[static_cast<int64_t>(bh) * kD + t];
         // the ones rows around every V stage: 16 x 128 bytes of E4M3 1.0 (0x38)
         const uint4 ones = make_uint4(0x38383838u, 0x38383838u, 0x38383838u, 0x38383838u);
@@ -342,7 +347,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
-        const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
         unsigned char *sMA = smem + kOffMA;
         unsigned char *sMB = smem + kOffMB;
         const float kNegInf = __int_as_float(0xff800000);
@@ -351,8 +355,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = true;
         if (par == 0) {
             // Q tile into TMEM (the A operand of QK): this row's 128 codes, 32 columns
-            load_q_row(p.q8 + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD,
-                       tl + kTmemQ);
+            VCA_TMEM_ST32(tl + kTmemQ, qv);
             tmem_st_wait();
             tc_fence_before();
             __syncwarp();
@@ -552,8 +555,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the tail blocks' means (fp32) in the mean-B buffer, whose last
             // reader (the final mean MMA) has finished
             float *sMu = reinterpret_cast<float *>(sMB);
-            for (int i = threadIdx.x - 64; i < rs_cnt * kD; i += 32 * kSoftmaxWarps)
-                sMu[i] = bf16_bits_to_f32(vmh[(tail0 + i / kD) * kD + (i % kD)]);
+            fill_tail_means(sMu, reinterpret_cast<const uint16_t *>(smem + kOffMean), tail0, rs_cnt, threadIdx.x - 64,
+                            32 * kSoftmaxWarps);
             bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             const float inv_l = 1.0f / sL[row];
             const int col0 = kCols * par;

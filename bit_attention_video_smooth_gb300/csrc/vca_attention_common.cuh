@@ -104,7 +104,9 @@ __device__ __forceinline__ void store_mean_row(unsigned char *dst, int row, cons
 // channels starting at col0: tO is the TMEM address of those accumulator
 // columns in this thread's lane, sMu the fp32 means [t][128] of the rs_cnt
 // blocks since the last mean MMA, whose row sums are in sRS slots
-// (slot0 + t) % kRsSlots; orow the output row at col0.
+// (slot0 + t) % kRsSlots; orow the output row at col0.  sSV and sMu are
+// 16-byte aligned and read four channels at a time (every thread of a warp
+// reads the same address: one broadcast per four channels).
 constexpr int kRsSlots = 32;   // row-sum slots per query row (a ring)
 __device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, const float *sRS, const float *sMu,
                                              int rs_cnt, int slot0, int row, int col0, float inv_l, uint16_t *orow) {
@@ -113,15 +115,28 @@ __device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, cons
         uint32_t o[32];
         VCA_TMEM_LD32(tO + 32 * i, o);
         tmem_ld_wait();
+        const float4 *sv4 = reinterpret_cast<const float4 *>(sSV + col0 + 32 * i);
         float acc[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) acc[e] = __fmul_rn(__uint_as_float(o[e]), sSV[col0 + 32 * i + e]);
+        for (int e = 0; e < 8; ++e) {
+            const float4 v = sv4[e];
+            acc[4 * e] = __fmul_rn(__uint_as_float(o[4 * e]), v.x);
+            acc[4 * e + 1] = __fmul_rn(__uint_as_float(o[4 * e + 1]), v.y);
+            acc[4 * e + 2] = __fmul_rn(__uint_as_float(o[4 * e + 2]), v.z);
+            acc[4 * e + 3] = __fmul_rn(__uint_as_float(o[4 * e + 3]), v.w);
+        }
 #pragma unroll 1
         for (int t = 0; t < rs_cnt; ++t) {
             const float r = sRS[((slot0 + t) & (kRsSlots - 1)) * kBlk + row];
-            const float *mu = sMu + t * kD + col0 + 32 * i;
+            const float4 *mu4 = reinterpret_cast<const float4 *>(sMu + t * kD + col0 + 32 * i);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) acc[e] = __fmaf_rn(r, mu[e], acc[e]);
+            for (int e = 0; e < 8; ++e) {
+                const float4 u = mu4[e];
+                acc[4 * e] = __fmaf_rn(r, u.x, acc[4 * e]);
+                acc[4 * e + 1] = __fmaf_rn(r, u.y, acc[4 * e + 1]);
+                acc[4 * e + 2] = __fmaf_rn(r, u.z, acc[4 * e + 2]);
+                acc[4 * e + 3] = __fmaf_rn(r, u.w, acc[4 * e + 3]);
+            }
         }
         uint32_t w[16];
 #pragma unroll
@@ -129,6 +144,20 @@ __device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, cons
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             reinterpret_cast<uint4 *>(orow + 32 * i)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+    }
+}
+
+// The fp32 means of the epilogue's tail blocks tail0 .. tail0 + rs_cnt - 1
+// into sMu [t][128], from the bf16 group buffers the V producer filled
+// (group g in buffer g & 1).  tail0 is a multiple of kMeanJ and rs_cnt is at
+// most kMeanJ + kMeanLag, so the tail spans groups tail0 / kMeanJ and the one
+// after it, the last two groups loaded: neither buffer has been refilled, and
+// PV of every block has completed, so every group's copy has landed.
+__device__ __forceinline__ void fill_tail_means(float *sMu, const uint16_t *sMean, int tail0, int rs_cnt, int tid,
+                                                int nthreads) {
+    for (int i = tid; i < rs_cnt * kD; i += nthreads) {
+        const int b = tail0 + i / kD;
+        sMu[i] = bf16_bits_to_f32(sMean[((b / kMeanJ) & 1) * (kMeanJ * kD) + (b % kMeanJ) * kD + (i % kD)]);
     }
 }
 
@@ -166,11 +195,10 @@ __device__ __forceinline__ void stage_means(int row, const float *sRS, const flo
     store_mean_row(sMB, row, hi, lo, false);
 }
 
-// Q tile row into TMEM (the A operand of QK): `row`'s 128 E4M3 codes as 32
-// columns at tq (this thread's lane).
-__device__ __forceinline__ void load_q_row(const uint8_t *q8row, uint32_t tq) {
+// One Q tile row (the A operand of QK) into registers: `row`'s 128 E4M3
+// codes as 32 words, in the column order of its TMEM lane.
+__device__ __forceinline__ void load_q_regs(const uint8_t *q8row, uint32_t (&qv)[32]) {
     const uint4 *qrow = reinterpret_cast<const uint4 *>(q8row);
-    uint32_t qv[32];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint4 u = qrow[i];
@@ -179,7 +207,6 @@ __device__ __forceinline__ void load_q_row(const uint8_t *q8row, uint32_t tq) {
         qv[4 * i + 2] = u.z;
         qv[4 * i + 3] = u.w;
     }
-    VCA_TMEM_ST32(tq, qv);
 }
 
 // ---------------------------------------------------------------------------

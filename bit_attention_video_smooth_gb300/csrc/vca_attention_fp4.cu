@@ -471,7 +471,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
         const float sqv = p.sq[static_cast<int64_t>(bh) * nb + qtile];
         const float *skh = p.sk + static_cast<int64_t>(bh) * nb;
-        const uint16_t *vmh = p.v_mean + static_cast<int64_t>(bh) * nb * kD;
         unsigned char *sMA = smem + kOffMA;
         unsigned char *sMB = smem + kOffMB;
         const float kNegInf = __int_as_float(0xff800000);
@@ -669,8 +668,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the tail blocks' means (fp32) in the mean-B buffer, whose last
             // reader (the final mean MMA) has finished
             float *sMu = reinterpret_cast<float *>(sMB);
-            for (int i = threadIdx.x - 64; i < rs_cnt * kD; i += 32 * kSoftmaxWarps)
-                sMu[i] = bf16_bits_to_f32(vmh[(tail0 + i / kD) * kD + (i % kD)]);
+            fill_tail_means(sMu, reinterpret_cast<const uint16_t *>(smem + kOffMean), tail0, rs_cnt, threadIdx.x - 64,
+                            32 * kSoftmaxWarps);
             bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
             const float inv_l = 1.0f / sL[row];
             const int col0 = kCols * par;
