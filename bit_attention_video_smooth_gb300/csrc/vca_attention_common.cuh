@@ -100,16 +100,12 @@ __device__ __forceinline__ void store_mean_row(unsigned char *dst, int row, cons
 }
 
 
-// O row part = (O_acc s_v + sum_t rs_t mu_t) / l for this thread's kCols
-// channels starting at col0: tO is the TMEM address of those accumulator
-// columns in this thread's lane, sMu the fp32 means [t][128] of the rs_cnt
-// blocks since the last mean MMA, whose row sums are in sRS slots
-// (slot0 + t) % kRsSlots; orow the output row at col0.  sSV and sMu are
-// 16-byte aligned and read four channels at a time (every thread of a warp
-// reads the same address: one broadcast per four channels).
+// O row part = O_acc s_v / l for this thread's kCols channels starting at
+// col0 (every block's mean term is in O_acc by then): tO is the TMEM address
+// of those accumulator columns in this thread's lane, orow the output row at
+// col0.  sSV is 16-byte aligned and read four channels at a time.
 constexpr int kRsSlots = 32;   // row-sum slots per query row (a ring)
-__device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, const float *sRS, const float *sMu,
-                                             int rs_cnt, int slot0, int row, int col0, float inv_l, uint16_t *orow) {
+__device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, int col0, float inv_l, uint16_t *orow) {
 #pragma unroll 1
     for (int i = 0; i < kCols / 32; ++i) {
         uint32_t o[32];
@@ -125,39 +121,12 @@ __device__ __forceinline__ void store_output(uint32_t tO, const float *sSV, cons
             acc[4 * e + 2] = __fmul_rn(__uint_as_float(o[4 * e + 2]), v.z);
             acc[4 * e + 3] = __fmul_rn(__uint_as_float(o[4 * e + 3]), v.w);
         }
-#pragma unroll 1
-        for (int t = 0; t < rs_cnt; ++t) {
-            const float r = sRS[((slot0 + t) & (kRsSlots - 1)) * kBlk + row];
-            const float4 *mu4 = reinterpret_cast<const float4 *>(sMu + t * kD + col0 + 32 * i);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float4 u = mu4[e];
-                acc[4 * e] = __fmaf_rn(r, u.x, acc[4 * e]);
-                acc[4 * e + 1] = __fmaf_rn(r, u.y, acc[4 * e + 1]);
-                acc[4 * e + 2] = __fmaf_rn(r, u.z, acc[4 * e + 2]);
-                acc[4 * e + 3] = __fmaf_rn(r, u.w, acc[4 * e + 3]);
-            }
-        }
         uint32_t w[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) w[e] = pack_bf16x2(__fmul_rn(acc[2 * e], inv_l), __fmul_rn(acc[2 * e + 1], inv_l));
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             reinterpret_cast<uint4 *>(orow + 32 * i)[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-    }
-}
-
-// The fp32 means of the epilogue's tail blocks tail0 .. tail0 + rs_cnt - 1
-// into sMu [t][128], from the bf16 group buffers the V producer filled
-// (group g in buffer g & 1).  tail0 is a multiple of kMeanJ and rs_cnt is at
-// most kMeanJ + kMeanLag, so the tail spans groups tail0 / kMeanJ and the one
-// after it, the last two groups loaded: neither buffer has been refilled, and
-// PV of every block has completed, so every group's copy has landed.
-__device__ __forceinline__ void fill_tail_means(float *sMu, const uint16_t *sMean, int tail0, int rs_cnt, int tid,
-                                                int nthreads) {
-    for (int i = tid; i < rs_cnt * kD; i += nthreads) {
-        const int b = tail0 + i / kD;
-        sMu[i] = bf16_bits_to_f32(sMean[((b / kMeanJ) & 1) * (kMeanJ * kD) + (b % kMeanJ) * kD + (i % kD)]);
     }
 }
 
@@ -172,27 +141,76 @@ __host__ __device__ constexpr bool flush_after(int b) {
     return b >= kMeanJ + kMeanLag && (b % kMeanJ) == kMeanLag;
 }
 
-// Operands of the mean-restore MMA for blocks b0 .. b0+15 (row / channel
-// `row`): A row = the row sums from their ring slots, each brought from the
-// reference max it was taken against to m; B row = mean / s_v.
+// Operands of the mean-restore MMA for blocks b0 .. b0+n-1, n <= kMeanJ (row /
+// channel `row`): A row = the row sums from their ring slots, each brought
+// from the reference max it was taken against to m; B row = mean / s_v; the
+// K entries of the kMeanJ - n missing blocks are zero in both.  sMeanGroup
+// holds the means of the group's blocks, block b0 + i at i * kD.
 __device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
                                             const uint16_t *sMeanGroup, const float *sSV, unsigned char *sMA,
-                                            unsigned char *sMB) {
+                                            unsigned char *sMB, int n = kMeanJ) {
     float hi[kMeanJ], lo[kMeanJ];
 #pragma unroll
     for (int i = 0; i < kMeanJ; ++i) {
-        const int slot = ((b0 + i) & (kRsSlots - 1)) * kBlk + row;
-        float rs = sRS[slot];
-        const float mt = sRSM[slot];
-        if (mt != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mt, m)));
-        split_bf16(rs, hi[i], lo[i]);
+        hi[i] = lo[i] = 0.0f;
+        if (i < n) {
+            const int slot = ((b0 + i) & (kRsSlots - 1)) * kBlk + row;
+            float rs = sRS[slot];
+            const float mt = sRSM[slot];
+            if (mt != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mt, m)));
+            split_bf16(rs, hi[i], lo[i]);
+        }
     }
     store_mean_row(sMA, row, hi, lo, true);
     const float inv_sv = 1.0f / sSV[row];
 #pragma unroll
-    for (int i = 0; i < kMeanJ; ++i)
-        split_bf16(__fmul_rn(bf16_bits_to_f32(sMeanGroup[i * kD + row]), inv_sv), hi[i], lo[i]);
+    for (int i = 0; i < kMeanJ; ++i) {
+        hi[i] = lo[i] = 0.0f;
+        if (i < n) split_bf16(__fmul_rn(bf16_bits_to_f32(sMeanGroup[i * kD + row]), inv_sv), hi[i], lo[i]);
+    }
     store_mean_row(sMB, row, hi, lo, false);
+}
+
+// The epilogue's mean terms: blocks tail0 .. tail0 + rs_cnt - 1 (those after
+// the last in-loop mean MMA's range; rs_cnt <= 2 kMeanJ) are added into O by
+// one more mean-restore MMA group, two when rs_cnt > kMeanJ, instead of on
+// CUDA cores (there every thread reads every mean: shared-memory broadcast
+// bound).  Called by all softmax threads once every PV has completed: the
+// even-block threads stage blocks tail0 .. tail0 + 15 into tiles0 (A, B), the
+// odd-block threads the rest into tiles1; tail0 is a multiple of kMeanJ, so
+// the two groups' means are in buffers (tail0 / kMeanJ) & 1 and the other.
+// One thread issues the MMAs and commits them to `bar` (phase 0, count 1);
+// every thread waits for it.  Returns false when that wait gave up (the
+// issuing thread then still waits for its MMAs, so that TMEM outlives them).
+__device__ __forceinline__ bool restore_tail_means(int par, int row, bool issuer, const float *sRS, const float *sRSM,
+                                                   float mf, int tail0, int rs_cnt, const uint16_t *sMean,
+                                                   const float *sSV, unsigned char *tiles0, unsigned char *tiles1,
+                                                   uint32_t tO, uint64_t *bar, int *abort_flag, uint64_t limit_ns) {
+    const int n0 = rs_cnt < kMeanJ ? rs_cnt : kMeanJ, n1 = rs_cnt - n0;
+    const int g0 = tail0 / kMeanJ;
+    constexpr uint32_t kTile = kBlk * kD;   // one staged operand: 128 rows x 64 bf16
+    if (par == 0)
+        stage_means(row, sRS, sRSM, mf, tail0, sMean + (g0 & 1) * (kMeanJ * kD), sSV, tiles0, tiles0 + kTile, n0);
+    else if (n1 > 0)
+        stage_means(row, sRS, sRSM, mf, tail0 + kMeanJ, sMean + ((g0 + 1) & 1) * (kMeanJ * kD), sSV, tiles1,
+                    tiles1 + kTile, n1);
+    fence_proxy_async_smem();   // read by the tensor core
+    bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
+    if (issuer) {
+        tc_fence_after();
+        constexpr uint32_t idesc_bf16 = make_idesc(128, 128, 1, 1);
+        for (int g = 0; g < (n1 > 0 ? 2 : 1); ++g) {
+            const uint32_t base = smem_u32(g == 0 ? tiles0 : tiles1);
+            const uint64_t da = sdesc_k_sw128(base), db = sdesc_k_sw128(base + kTile);
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) mma_f16(tO, da + 2 * kk, db + 2 * kk, idesc_bf16, 1u);
+        }
+        tc_commit(bar);
+    }
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(bar, 0, abort_flag, limit_ns));
+    if (!ok && issuer) drain_wait(bar, 0, limit_ns);
+    if (ok) tc_fence_after();
+    return ok;
 }
 
 // One Q tile row (the A operand of QK) into registers: `row`'s 128 E4M3

@@ -97,7 +97,7 @@ constexpr uint32_t kOffMX = kOffSV + kBlk * 4;               // fp32 [2][128] re
 constexpr uint32_t kOffL = kOffMX + 2 * kBlk * 4;            // fp32 [128] l, [2][128] partial l, [2][128] their max
 constexpr uint32_t kOffLg = kOffL + 5 * kBlk * 4;            // fp32 [128]: -log2(dec(E4M3 code)), -inf for code 0
 constexpr uint32_t kOffBar = kOffLg + kBlk * 4;
-constexpr int kNumBars = 1 + 2 * kKStages + 3 * kVStages + 2 * 4 + 2;
+constexpr int kNumBars = 1 + 2 * kKStages + 3 * kVStages + 2 * 4 + 2 + 1;
 constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;       // tmem address, abort flag
 constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;       // + alignment slack
 static_assert(kOffQ % 1024 == 0 && kOffV % 1024 == 0 && kVStageBytes % 1024 == 0 && kOffOnes % 1024 == 0 && kOffMA % 1024 == 0 &&
@@ -143,7 +143,7 @@ __device__ __forceinline__ void tc_cp_rows_x4(uint32_t taddr, uint64_t sdesc) {
 }
 
 struct Bars {
-    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_ready, *v_empty, *s_full, *s_free, *p_full, *pv_done, *drain;
+    uint64_t *q_full, *k_full, *k_empty, *v_full, *v_ready, *v_empty, *s_full, *s_free, *p_full, *pv_done, *drain, *tail;
 };
 
 struct Params {
@@ -251,6 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     B.p_full = B.s_free + 2;
     B.pv_done = B.p_full + 2;
     B.drain = B.pv_done + 2;   // [0]: QK thread, [1]: PV thread
+    B.tail = B.drain + 2;      // the epilogue's mean-restore MMAs
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     int *abort_flag = reinterpret_cast<int *>(smem + kOffMisc + 4);
     float *sRS = reinterpret_cast<float *>(smem + kOffRS);
@@ -284,6 +285,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(B.pv_done + i, 1);
             mbar_init(B.drain + i, 1);
         }
+        mbar_init(B.tail, 1);
         *abort_flag = 0;
         mbar_fence_init();
     }
@@ -648,7 +650,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the blocks after the last mean MMA's range
             const int bf = nb - 1 >= kMeanJ + kMeanLag ? kMeanLag + kMeanJ * ((nb - 1 - kMeanLag) / kMeanJ) : -1;
             const int tail0 = bf >= 0 ? bf - kMeanLag : 0;
-            const int rs_cnt = nb - tail0;
             const float mf = sMp[((nb - 1) & 1) * kBlk + row];   // the final reference max
             if (par == 0) {
                 float lt = 0.0f;
@@ -660,21 +661,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                     : __fmul_rn(sLp[q * kBlk + row], ex2_approx(__fsub_rn(mq, mf))));
                 }
                 sL[row] = lt;
-                for (int t = 0; t < rs_cnt; ++t) {
-                    const int slot = ((tail0 + t) & (kRsSlots - 1)) * kBlk + row;
-                    if (sRSM[slot] != mf) sRS[slot] = __fmul_rn(sRS[slot], ex2_approx(__fsub_rn(sRSM[slot], mf)));
-                }
             }
-            // the tail blocks' means (fp32) in the mean-B buffer, whose last
-            // reader (the final mean MMA) has finished
-            float *sMu = reinterpret_cast<float *>(sMB);
-            fill_tail_means(sMu, reinterpret_cast<const uint16_t *>(smem + kOffMean), tail0, rs_cnt, threadIdx.x - 64,
-                            32 * kSoftmaxWarps);
-            bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
+            // the tail's mean terms by the tensor core: staged into the mean
+            // tiles (whose last reader, the final in-loop mean MMA, has
+            // finished) and the K ring's first two tiles (every QK has
+            // completed); sL is written before the staging barrier
+            ok = restore_tail_means(par, row, warp == 2 && lane == 0, sRS, sRSM, mf, tail0, nb - tail0,
+                                    reinterpret_cast<const uint16_t *>(smem + kOffMean), sSV, sMA, smem + kOffK,
+                                    tl + kTmemO, B.tail, abort_flag, p.limit_ns);
+        }
+        if (ok) {
             const float inv_l = 1.0f / sL[row];
             const int col0 = kCols * par;
             uint16_t *orow = p.O + (static_cast<int64_t>(bh) * N + static_cast<int64_t>(qtile) * kBlk + row) * kD + col0;
-            store_output(tl + kTmemO + col0, sSV, sRS, sMu, rs_cnt, tail0, row, col0, inv_l, orow);
+            store_output(tl + kTmemO + col0, sSV, col0, inv_l, orow);
         }
     }
 

@@ -83,8 +83,9 @@ def test_e4m3_shared_memory_layout(e4m3):
     assert c["kOffMean"] % 16 == 0 and c["kOffRS"] - c["kOffMean"] == 2 * c["kMeanGroupBytes"]
     assert c["kMeanGroupBytes"] == c["kMeanJ"] * 128 * 2
     assert c["kOffRSM"] - c["kOffRS"] == c["kRsSlots"] * 128 * 4
-    # one mbarrier each: q_full, K and V full/empty rings, s_full, s_free, p_full, pv_done, drain (two each)
-    assert c["kNumBars"] == 1 + 2 * c["kKStages"] + 2 * c["kVStages"] + 2 * 5
+    # one mbarrier each: q_full, K and V full/empty rings, s_full, s_free, p_full, pv_done, drain (two each),
+    # the epilogue's tail MMAs
+    assert c["kNumBars"] == 1 + 2 * c["kKStages"] + 2 * c["kVStages"] + 2 * 5 + 1
 
 
 def test_nvfp4_tmem_plan(nvfp4):
@@ -103,9 +104,9 @@ def test_nvfp4_tmem_plan(nvfp4):
     _disjoint(cols, c["kTmemCols"])
     # the row-sum MMA writes N = 16 columns into a slot of 16
     assert c["kOnesRows"] == 16
-    # 32 mbarriers' worth of roles: Q, the K ring, the V ring (landed, laid
-    # out, released), S / P / PV per parity and the two issuers' drains
-    assert c["kNumBars"] == 1 + 2 * c["kKStages"] + 3 * c["kVStages"] + 2 * 5
+    # mbarriers for Q, the K ring, the V ring (landed, laid out, released),
+    # S / P / PV per parity, the two issuers' drains and the epilogue's tail MMAs
+    assert c["kNumBars"] == 1 + 2 * c["kKStages"] + 3 * c["kVStages"] + 2 * 5 + 1
 
 
 def test_nvfp4_shared_memory_layout(nvfp4):

@@ -6,14 +6,15 @@ shared-memory slots (block j in slot j % kRsSlots): the thread of the block's
 parity writes it at block j + 2, once PV(j) is done.  After PV(b), for every b
 with flush_after(b), one MMA adds the terms of blocks b - kMeanJ - kMeanLag ..
 b - kMeanLag - 1, staged by the thread of block b; the blocks after the last
-such range are added in the epilogue.  What must hold:
+such range (the tail) are added in the epilogue by one more MMA group, two
+when the tail is longer than kMeanJ.  What must hold:
   * the MMA ranges and the epilogue's tail cover every block exactly once;
   * every row sum an MMA stages is visible to the staging thread: its own
     parity's sums were written by itself earlier, the partner's before a
     reference-max hand-over that thread has already received;
   * no slot is overwritten while its entry is still to be read (by a later MMA
     or the epilogue);
-  * the epilogue's tail fits the fp32 staging it uses (the mean-B tile).
+  * the epilogue's tail fits the two operand groups it is staged into.
 The constants and the flush rule are read from the kernel source, so the model
 follows the kernel.
 """
@@ -45,6 +46,8 @@ def K(request):
     assert "const int b0 = b - kMeanJ - kMeanLag;" in kern
     assert "stage_means(row, sRS, sRSM, m_new, b0," in kern
     assert "if (flush_after(j))" in kern and "if (ok && flush_after(b))" in kern
+    assert "ok = restore_tail_means(par, row, warp == 2 && lane == 0, sRS, sRSM, mf, tail0, nb - tail0," in kern
+    assert "const int n0 = rs_cnt < kMeanJ ? rs_cnt : kMeanJ, n1 = rs_cnt - n0;" in common
     return {"J": _const(common, "kMeanJ"), "L": _const(common, "kMeanLag"), "S": _const(common, "kRsSlots"),
             "blk": 128, "d": 128, "tile_bytes": 128 * 128}
 
@@ -126,7 +129,12 @@ def test_epilogue_tail_fits_its_staging(K):
     for nb in range(1, 600):
         _, tail0 = schedule(K, nb)
         worst = max(worst, nb - tail0)
-    # the tail's means are staged as fp32 [rs_cnt][d] in the mean-B tile
-    assert worst * K["d"] * 4 <= K["tile_bytes"], worst
+        # the tail starts a means group (its first kMeanJ blocks share one
+        # group buffer, the rest the next one) and both its groups are the
+        # last two loaded, so neither buffer has been refilled
+        assert tail0 % K["J"] == 0, nb
+        assert (nb - 1) // K["J"] - tail0 // K["J"] <= 1, nb
+    # the tail is staged as at most two operand groups of kMeanJ blocks
+    assert worst <= 2 * K["J"], worst
     assert worst <= K["S"]
     assert worst == K["J"] + K["L"]
