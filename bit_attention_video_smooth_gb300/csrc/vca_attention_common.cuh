@@ -146,9 +146,8 @@ __host__ __device__ constexpr bool flush_after(int b) {
 // from the reference max it was taken against to m; B row = mean / s_v; the
 // K entries of the kMeanJ - n missing blocks are zero in both.  sMeanGroup
 // holds the means of the group's blocks, block b0 + i at i * kD.
-__device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
-                                            const uint16_t *sMeanGroup, const float *sSV, unsigned char *sMA,
-                                            unsigned char *sMB, int n = kMeanJ) {
+__device__ __forceinline__ void stage_mean_sums(int row, const float *sRS, const float *sRSM, float m, int b0,
+                                                unsigned char *sMA, int n = kMeanJ) {
     float hi[kMeanJ], lo[kMeanJ];
 #pragma unroll
     for (int i = 0; i < kMeanJ; ++i) {
@@ -162,6 +161,10 @@ __device__ __forceinline__ void stage_means(int row, const float *sRS, const flo
         }
     }
     store_mean_row(sMA, row, hi, lo, true);
+}
+__device__ __forceinline__ void stage_mean_values(int row, const uint16_t *sMeanGroup, const float *sSV,
+                                                  unsigned char *sMB, int n = kMeanJ) {
+    float hi[kMeanJ], lo[kMeanJ];
     const float inv_sv = 1.0f / sSV[row];
 #pragma unroll
     for (int i = 0; i < kMeanJ; ++i) {
@@ -170,15 +173,22 @@ __device__ __forceinline__ void stage_means(int row, const float *sRS, const flo
     }
     store_mean_row(sMB, row, hi, lo, false);
 }
+__device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
+                                            const uint16_t *sMeanGroup, const float *sSV, unsigned char *sMA,
+                                            unsigned char *sMB) {
+    stage_mean_sums(row, sRS, sRSM, m, b0, sMA);
+    stage_mean_values(row, sMeanGroup, sSV, sMB);
+}
 
 // The epilogue's mean terms: blocks tail0 .. tail0 + rs_cnt - 1 (those after
 // the last in-loop mean MMA's range; rs_cnt <= 2 kMeanJ) are added into O by
 // one more mean-restore MMA group, two when rs_cnt > kMeanJ, instead of on
 // CUDA cores (there every thread reads every mean: shared-memory broadcast
-// bound).  Called by all softmax threads once every PV has completed: the
-// even-block threads stage blocks tail0 .. tail0 + 15 into tiles0 (A, B), the
-// odd-block threads the rest into tiles1; tail0 is a multiple of kMeanJ, so
-// the two groups' means are in buffers (tail0 / kMeanJ) & 1 and the other.
+// bound).  Called by all softmax threads once every PV has completed: blocks
+// tail0 .. tail0 + 15 go to tiles0 (A, B), the rest to tiles1; the even-block
+// threads stage the A rows (row sums), the odd-block threads the B rows
+// (means).  tail0 is a multiple of kMeanJ, so the two groups' means are in
+// buffers (tail0 / kMeanJ) & 1 and the other.
 // One thread issues the MMAs and commits them to `bar` (phase 0, count 1);
 // every thread waits for it.  Returns false when that wait gave up (the
 // issuing thread then still waits for its MMAs, so that TMEM outlives them).
@@ -189,11 +199,13 @@ __device__ __forceinline__ bool restore_tail_means(int par, int row, bool issuer
     const int n0 = rs_cnt < kMeanJ ? rs_cnt : kMeanJ, n1 = rs_cnt - n0;
     const int g0 = tail0 / kMeanJ;
     constexpr uint32_t kTile = kBlk * kD;   // one staged operand: 128 rows x 64 bf16
-    if (par == 0)
-        stage_means(row, sRS, sRSM, mf, tail0, sMean + (g0 & 1) * (kMeanJ * kD), sSV, tiles0, tiles0 + kTile, n0);
-    else if (n1 > 0)
-        stage_means(row, sRS, sRSM, mf, tail0 + kMeanJ, sMean + ((g0 + 1) & 1) * (kMeanJ * kD), sSV, tiles1,
-                    tiles1 + kTile, n1);
+    if (par == 0) {
+        stage_mean_sums(row, sRS, sRSM, mf, tail0, tiles0, n0);
+        if (n1 > 0) stage_mean_sums(row, sRS, sRSM, mf, tail0 + kMeanJ, tiles1, n1);
+    } else {
+        stage_mean_values(row, sMean + (g0 & 1) * (kMeanJ * kD), sSV, tiles0 + kTile, n0);
+        if (n1 > 0) stage_mean_values(row, sMean + ((g0 + 1) & 1) * (kMeanJ * kD), sSV, tiles1 + kTile, n1);
+    }
     fence_proxy_async_smem();   // read by the tensor core
     bar_sync(kBarSoftmax, 32 * kSoftmaxWarps);
     if (issuer) {

@@ -359,8 +359,9 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint16_t h) { return __uint_as
 
 // Two fp32 values -> two bf16 (round to nearest even); `lo` in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(lo))) |
-           (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(hi))) << 16);
+    uint32_t d;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+    return d;
 }
 
 // hi + lo split of x for two bf16 operands: hi = bf16(x), lo = x - hi (exact
