@@ -82,16 +82,12 @@ __device__ __forceinline__ void bar_arrive_release(uint32_t id, uint32_t count) 
 // into the 128-byte-swizzled K-major tile `dst`:
 //   A (query row): [hi | lo | hi | lo]   (chunks 0,1 hi; 2,3 lo; 4,5 hi; 6,7 lo)
 //   B (channel):   [hi | hi | lo | lo]   (chunks 0-3 hi; 4-7 lo)
-__device__ __forceinline__ void store_mean_row(unsigned char *dst, int row, const float (&hi)[kMeanJ],
-                                               const float (&lo)[kMeanJ], bool a_operand) {
-    uint4 hv[2], lv[2];
+__device__ __forceinline__ void store_mean_row(unsigned char *dst, int row, const float (&x)[kMeanJ], bool a_operand) {
+    uint32_t h[kMeanJ / 2], l[kMeanJ / 2];
 #pragma unroll
-    for (int g = 0; g < 2; ++g) {
-        hv[g] = make_uint4(pack_bf16x2(hi[8 * g + 0], hi[8 * g + 1]), pack_bf16x2(hi[8 * g + 2], hi[8 * g + 3]),
-                           pack_bf16x2(hi[8 * g + 4], hi[8 * g + 5]), pack_bf16x2(hi[8 * g + 6], hi[8 * g + 7]));
-        lv[g] = make_uint4(pack_bf16x2(lo[8 * g + 0], lo[8 * g + 1]), pack_bf16x2(lo[8 * g + 2], lo[8 * g + 3]),
-                           pack_bf16x2(lo[8 * g + 4], lo[8 * g + 5]), pack_bf16x2(lo[8 * g + 6], lo[8 * g + 7]));
-    }
+    for (int k = 0; k < kMeanJ / 2; ++k) split_pack_bf16x2(x[2 * k], x[2 * k + 1], h[k], l[k]);
+    const uint4 hv[2] = {make_uint4(h[0], h[1], h[2], h[3]), make_uint4(h[4], h[5], h[6], h[7])};
+    const uint4 lv[2] = {make_uint4(l[0], l[1], l[2], l[3]), make_uint4(l[4], l[5], l[6], l[7])};
 #pragma unroll
     for (int ck = 0; ck < 8; ++ck) {
         const bool use_lo = a_operand ? (((ck >> 1) & 1) != 0) : (ck >= 4);
@@ -148,30 +144,28 @@ __host__ __device__ constexpr bool flush_after(int b) {
 // holds the means of the group's blocks, block b0 + i at i * kD.
 __device__ __forceinline__ void stage_mean_sums(int row, const float *sRS, const float *sRSM, float m, int b0,
                                                 unsigned char *sMA, int n = kMeanJ) {
-    float hi[kMeanJ], lo[kMeanJ];
+    float x[kMeanJ];
 #pragma unroll
     for (int i = 0; i < kMeanJ; ++i) {
-        hi[i] = lo[i] = 0.0f;
+        x[i] = 0.0f;
         if (i < n) {
             const int slot = ((b0 + i) & (kRsSlots - 1)) * kBlk + row;
             float rs = sRS[slot];
             const float mt = sRSM[slot];
             if (mt != m) rs = __fmul_rn(rs, ex2_approx(__fsub_rn(mt, m)));
-            split_bf16(rs, hi[i], lo[i]);
+            x[i] = rs;
         }
     }
-    store_mean_row(sMA, row, hi, lo, true);
+    store_mean_row(sMA, row, x, true);
 }
 __device__ __forceinline__ void stage_mean_values(int row, const uint16_t *sMeanGroup, const float *sSV,
                                                   unsigned char *sMB, int n = kMeanJ) {
-    float hi[kMeanJ], lo[kMeanJ];
+    float x[kMeanJ];
     const float inv_sv = 1.0f / sSV[row];
 #pragma unroll
-    for (int i = 0; i < kMeanJ; ++i) {
-        hi[i] = lo[i] = 0.0f;
-        if (i < n) split_bf16(__fmul_rn(bf16_bits_to_f32(sMeanGroup[i * kD + row]), inv_sv), hi[i], lo[i]);
-    }
-    store_mean_row(sMB, row, hi, lo, false);
+    for (int i = 0; i < kMeanJ; ++i)
+        x[i] = i < n ? __fmul_rn(bf16_bits_to_f32(sMeanGroup[i * kD + row]), inv_sv) : 0.0f;
+    store_mean_row(sMB, row, x, false);
 }
 __device__ __forceinline__ void stage_means(int row, const float *sRS, const float *sRSM, float m, int b0,
                                             const uint16_t *sMeanGroup, const float *sSV, unsigned char *sMA,

@@ -370,6 +370,14 @@ __device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
     hi = __bfloat162float(__float2bfloat16_rn(x));
     lo = __fsub_rn(x, hi);
 }
+// The same split of two values, packed: h = bf16(a) | bf16(b) << 16 and
+// l = bf16(a - hi(a)) | bf16(b - hi(b)) << 16 (one conversion per word; the
+// hi halves are read back as fp32 by placing them in the high 16 bits).
+__device__ __forceinline__ void split_pack_bf16x2(float a, float b, uint32_t &h, uint32_t &l) {
+    h = pack_bf16x2(a, b);
+    const float ha = __uint_as_float(h << 16), hb = __uint_as_float(h & 0xffff0000u);
+    l = pack_bf16x2(__fsub_rn(a, ha), __fsub_rn(b, hb));
+}
 
 // Two fp32 values -> two E4M3 bytes (round to nearest even, saturate to 448);
 // `lo` lands in the low byte.

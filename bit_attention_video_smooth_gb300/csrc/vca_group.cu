@@ -154,13 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         uint32_t wh[4], wl[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            float h0, l0, h1, l1;
-            split_bf16(v[2 * e], h0, l0);
-            split_bf16(v[2 * e + 1], h1, l1);
-            wh[e] = pack_bf16x2(h0, h1);
-            wl[e] = pack_bf16x2(l0, l1);
-        }
+        for (int e = 0; e < 4; ++e) split_pack_bf16x2(v[2 * e], v[2 * e + 1], wh[e], wl[e]);
         unsigned char *panel = smem + L::kOffB + (x0 / 64) * L::kBPanel;
         const uint32_t chunk16 = (x0 % 64) / 8;
         *reinterpret_cast<uint4 *>(panel + sw128_offset(c, chunk16)) = make_uint4(wh[0], wh[1], wh[2], wh[3]);
