@@ -134,16 +134,21 @@ template <bool kExpcast, int kOff, int kW>
 __device__ __forceinline__ void codes32(const uint32_t (&X)[kCols], float c, float m, bool fast, uint32_t one,
                                         uint32_t (&W)[32]) {
     if constexpr (kExpcast) {
-        // t / 256 = fma(S, 8c / 256, (55.65 - 8m) / 256), both scalings exact
-        const float c8s = __fmul_rn(c, 1.0f / 32.0f);
-        const float bs = __fmul_rn(__fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m)), 1.0f / 256.0f);
+        // t = fma(S, 8c, 55.65 - 8m); the clipped form takes t / 256 (both
+        // scalings exact)
+        const float c8 = __fmul_rn(8.0f, c);
+        const float b = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m));
         if (fast) {
+            const uint64_t c8x2 = pk2(__float_as_uint(c8), __float_as_uint(c8));
+            const uint64_t bx2 = pk2(__float_as_uint(b), __float_as_uint(b));
 #pragma unroll
             for (int q = 0; q < 8; ++q) {
                 const uint32_t sv[4] = {X[kOff + 4 * q], X[kOff + 4 * q + 1], X[kOff + 4 * q + 2], X[kOff + 4 * q + 3]};
-                W[kW + q] = expcast4<false>(sv, c8s, bs, one);
+                W[kW + q] = expcast4_fast(sv, c8x2, bx2, one);
             }
         } else {
+            const float c8s = __fmul_rn(c8, 1.0f / 256.0f);
+            const float bs = __fmul_rn(b, 1.0f / 256.0f);
             // copies, so that X and W themselves never need an address
             uint32_t sv[32], w[8];
 #pragma unroll
@@ -584,22 +589,26 @@ __global__ void expcast_codes_kernel(const float *__restrict__ s_raw, const floa
                                      const float *__restrict__ m, int64_t n, uint8_t *__restrict__ out) {
     for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; 4 * g < n;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        // the kernel's arithmetic, one scale per element: t / 256 from the
-        // exactly scaled factors
+        // the kernel's arithmetic, one scale per element: 8c and 55.65 - 8m,
+        // and for the clipped form t / 256 from the exactly scaled factors
         uint32_t w = 0;
         bool fast = true;
         uint32_t sv[4];
-        float c8s[4], bs[4];
+        float c8[4], b[4];
         for (int e = 0; e < 4; ++e) {
             const int64_t i = (4 * g + e < n) ? 4 * g + e : n - 1;
             sv[e] = __float_as_uint(s_raw[i]);
-            c8s[e] = __fmul_rn(c[i], 1.0f / 32.0f);
-            bs[e] = __fmul_rn(__fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m[i])), 1.0f / 256.0f);
+            c8[e] = __fmul_rn(8.0f, c[i]);
+            b[e] = __fsub_rn(kExpcastOffset, __fmul_rn(8.0f, m[i]));
             fast = fast && fabsf(m[i]) < kExpcastFastMax && __fmul_rn(s_raw[i], c[i]) <= __fadd_rn(m[i], 8.0f);
         }
         for (int e = 0; e < 4; ++e) {
             const uint32_t one[4] = {sv[e], sv[e], sv[e], sv[e]};
-            const uint32_t code = (fast ? expcast4<false>(one, c8s[e], bs[e], 1u) : expcast4<true>(one, c8s[e], bs[e], 1u)) & 0xFFu;
+            const uint32_t code =
+                (fast ? expcast4_fast(one, pk2(__float_as_uint(c8[e]), __float_as_uint(c8[e])),
+                                      pk2(__float_as_uint(b[e]), __float_as_uint(b[e])), 1u)
+                      : expcast4<true>(one, __fmul_rn(c8[e], 1.0f / 256.0f), __fmul_rn(b[e], 1.0f / 256.0f), 1u)) &
+                0xFFu;
             w |= code << (8 * e);
         }
         for (int e = 0; e < 4; ++e)

@@ -504,6 +504,34 @@ __device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
     return d;
 }
 
+// Four ExpCast codes packed in one word (byte i = element i) when every code
+// is at most 126 (|m| < 2^22 and fp32(s c) <= fp32(m + 8), as for expcast4<false>),
+// in nine instructions:
+//   t = fma(s, 8c, 55.65 - 8m)            two packed FMAs (t with its one rounding)
+//   y = t * 2^-149                         two packed multiplies: the exact product
+//       rounds, nearest even, to a multiple of the smallest subnormal, so y's
+//       bit pattern is rne(t) for 0 <= t < 2^23, and a negative t leaves the
+//       sign bit set (a negative 32-bit integer)
+//   cvt.pack.sat.u8.s32.b32 twice         clamps each pattern to [0, 255] as a
+//       signed integer and packs it: d = (c & 0xffff) << 16 | sat(a) << 8 | sat(b)
+//       (the layout measured on the device)
+//   the flush of codes 1..7 as in expcast4.
+// Subnormal results are kept: neither the multiply nor the FMA flushes to zero.
+__device__ __forceinline__ uint32_t expcast4_fast(const uint32_t (&s)[4], uint64_t c8x2, uint64_t bx2, uint32_t one) {
+    const uint64_t tiny2 = pk2(1u, 1u);   // 2^-149 in both halves
+    const uint64_t y01 = mul2(fma2(pk2(s[0], s[1]), c8x2, bx2), tiny2);
+    const uint64_t y23 = mul2(fma2(pk2(s[2], s[3]), c8x2, bx2), tiny2);
+    uint32_t y[4];
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(y[0]), "=r"(y[1]) : "l"(y01));
+    asm("mov.b64 {%0, %1}, %2;" : "=r"(y[2]), "=r"(y[3]) : "l"(y23));
+    uint32_t hi, w;
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(hi) : "r"(y[3]), "r"(y[2]), "r"(0u));
+    asm("cvt.pack.sat.u8.s32.b32 %0, %1, %2, %3;" : "=r"(w) : "r"(y[1]), "r"(y[0]), "r"(hi));
+    uint32_t t;
+    asm("mad.lo.u32 %0, %1, %2, 2021161080;" : "=r"(t) : "r"(w), "r"(one));   // w + 0x78787878
+    return w & prmt(t, 0u, 0xBA98);
+}
+
 __device__ __forceinline__ float ex2_approx(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));

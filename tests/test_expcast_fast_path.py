@@ -1,8 +1,19 @@
-"""The arithmetic behind the attention kernel's ExpCast fast path, checked on
-the CPU (the GPU tests compare the device codes with the oracle bit for bit on
+"""The arithmetic behind the attention kernel's ExpCast codes, checked on the
+CPU (the GPU tests compare the device codes with the oracle bit for bit on
 millions of inputs; these checks cover every value the steps can see).
 
-Per element the kernel forms u = sat(fma(s, 8c/256, (55.65 - 8m)/256)), which
+Fast path (every code at most 126; nine instructions per four codes): the
+kernel forms the oracle's t = fma(s, 8c, 55.65 - 8m) in fp32 (packed, two at a
+time), multiplies it by 2^-149, the smallest subnormal (packed): the exact
+product rounds, nearest even, to a multiple of 2^-149, so the product's bit
+pattern is rne(t) for 0 <= t < 2^23 and has the sign bit set for t < 0; then
+`cvt.pack.sat.u8.s32.b32` (d = (c & 0xffff) << 16 | sat(a) << 8 | sat(b), each
+operand clamped to [0, 255] as a signed integer; the layout measured on the
+device) packs two such patterns per instruction, and the flush below zeroes
+codes 1..7.
+
+Clipped form (taken only for |m| >= 2^22): per element the kernel forms
+u = sat(fma(s, 8c/256, (55.65 - 8m)/256)), which
 is t/256 for the oracle's t = fma(s, 8c, 55.65 - 8m) (a power-of-two scaling
 changes no rounding), clamped to [0, 1].  It then
   1. adds 1.5 * 2^15 in fp32: the sum's unit in the last place is 2^-8, so its
@@ -14,7 +25,7 @@ changes no rounding), clamped to [0, 1].  It then
      its code is >= 8 (no carry crosses bytes for codes <= 126), and a byte
      permute with sign replication (selector 0xBA98) turns those bits into a
      byte mask.
-The fast path skips the clip at 126; that is safe when fp32(s c) <= fp32(m + 8)
+The fast path has no clip at 126; that is safe when fp32(s c) <= fp32(m + 8)
 and |m| < 2^22 (the lazy reference max is never more than 8 below the block
 max), because t then stays below 126.5.
 """
@@ -86,6 +97,70 @@ def test_packing_and_flush_of_every_code_in_every_lane():
     assert prmt(0x44332211, 0x88776655, 0x3210) == 0x44332211
     assert prmt(0x44332211, 0x88776655, 0x7654) == 0x88776655
     assert prmt(0x00800180, 0, 0xBA98) == 0x00FF00FF
+
+
+TINY = np.float32(2.0 ** -149)
+
+
+def cvt_pack_sat_u8(a, b, c):
+    """cvt.pack.sat.u8.s32.b32 d, a, b, c: a and b as signed 32-bit integers
+    clamped to [0, 255], d = (c & 0xffff) << 16 | sat(a) << 8 | sat(b)."""
+    def sat(v):
+        v = int(v) & M32
+        v = v - (1 << 32) if v & 0x80000000 else v
+        return min(max(v, 0), 255)
+    return ((int(c) & 0xFFFF) << 16) | (sat(a) << 8) | sat(b)
+
+
+def fast_codes(t4):
+    """The fast path from four fp32 t values: patterns of t * 2^-149, two packs,
+    the flush."""
+    y = [int((np.float32(t) * TINY).view(np.uint32)) for t in t4]
+    hi = cvt_pack_sat_u8(y[3], y[2], 0)
+    w = cvt_pack_sat_u8(y[1], y[0], hi)
+    tt = (w * 1 + 0x78787878) & M32
+    return w & prmt(tt, 0, 0xBA98)
+
+
+def test_subnormal_multiply_rounds_t_to_the_code():
+    """Every fp32 t in [2^-10, 127): the bit pattern of fp32(t * 2^-149) is
+    rne(t); every t in (-2^12, 0) gives a pattern with the sign bit set (a
+    negative integer, which the pack clamps to 0); so does -0."""
+    for e in range(-10, 7):
+        base = (e + 127) << 23
+        t = np.arange(base, base + (1 << 23), dtype=np.uint32).view(np.float32)
+        t = t[t < np.float32(127.0)]
+        bits = (t * TINY).view(np.uint32)
+        want = np.rint(t.astype(np.float64)).astype(np.uint32)   # half to even
+        assert np.array_equal(bits, want), e
+    neg = -np.arange(1, 1 << 20, dtype=np.float32) / np.float32(256.0)
+    assert np.all(((neg * TINY).view(np.uint32) & 0x80000000) != 0)
+    assert (np.float32(-0.0) * TINY).view(np.uint32) == 0x80000000
+    # halves go to the even neighbour
+    for t, r in ((0.5, 0), (1.5, 2), (2.5, 2), (7.5, 8), (125.5, 126), (33.5, 34), (34.5, 34)):
+        assert int((np.float32(t) * TINY).view(np.uint32)) == r
+
+
+def test_fast_path_pack_and_flush_of_every_code_in_every_lane():
+    """Four t values -> the word of their flushed codes, for every code in every
+    lane, negative t (code 0) included."""
+    rng = np.random.default_rng(2)
+    def word(ts):
+        codes = [0 if t < 0 else int(np.rint(np.float64(t))) for t in ts]
+        return flushed_word(codes)
+    for lane in range(4):
+        for code in range(127):
+            ts = [float(x) for x in rng.uniform(-40, 126.4, 4).astype(np.float32)]
+            ts[lane] = float(np.float32(code + rng.uniform(-0.49, 0.49)))
+            assert fast_codes(ts) == word(ts), (lane, ts)
+    for _ in range(20000):
+        ts = [float(x) for x in rng.uniform(-300, 126.4, 4).astype(np.float32)]
+        assert fast_codes(ts) == word(ts), ts
+    # the pack's measured layout and saturation
+    assert cvt_pack_sat_u8(1, 2, 0) == 0x0102
+    assert cvt_pack_sat_u8(300, -7, 0) == 0xFF00
+    assert cvt_pack_sat_u8(7, 8, 0xAABBCCDD) == 0xCCDD0708
+    assert cvt_pack_sat_u8(0xFFFFFFFF, 128, 0xABCD) == 0xABCD0080
 
 
 def _fma_f32(a, b, c):
