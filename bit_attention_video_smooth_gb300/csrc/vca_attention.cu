@@ -423,14 +423,24 @@ __global__ void __launch_bounds__(kThreads, 1)
             // the next block's key scale, loaded after the hand-over so that the
             // fence before it never waits for this load
             if (b + 2 < nb) sk_next = skh[b + 2];
-            if (!__all_sync(0xffffffffu, valid)) {
-                ok = false;
-                break;
-            }
             // all 128 codes into registers: columns 64..127 from X while
-            // columns 0..63 are reloaded behind them
+            // columns 0..63 are reloaded behind them.  The ExpCast build takes
+            // the give-up test from the fast-path vote (one vote per block).
+            bool fast;
+            if constexpr (kExpcast) {
+                fast = __all_sync(0xffffffffu, valid && fabsf(m_new) < kExpcastFastMax);
+                if (!fast && !__all_sync(0xffffffffu, valid)) {
+                    ok = false;
+                    break;
+                }
+            } else {
+                fast = true;
+                if (!__all_sync(0xffffffffu, valid)) {
+                    ok = false;
+                    break;
+                }
+            }
             const uint32_t tp = tl + kTmemP0 + 32 * sb;
-            const bool fast = __all_sync(0xffffffffu, fabsf(m_new) < kExpcastFastMax);
             uint32_t W[32];
             codes32<kExpcast, 0, 16>(X, c, m_new, fast, p.one, W);
             VCA_TMEM_LD32(tS, X);
