@@ -206,7 +206,7 @@ __device__ __forceinline__ uint32_t nvfp4_scales4(const float (&gm)[kBlk / 16], 
         const uint64_t q0 = mul2(a2, r6);
         upk2(fma2(fma2(q0, m6, a2), r6, q0), q[i], q[i + 1]);
     }
-    const uint32_t sfa = (e4m3x2(q[0], q[1]) & 0xFFFFu) | (e4m3x2(q[2], q[3]) << 16);
+    const uint32_t sfa = e4m3x4(q[0], q[1], q[2], q[3]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) bias[kB + i] = __fadd_rn(sLg[(sfa >> (8 * i)) & 0xFFu], negm);
     return sfa;
