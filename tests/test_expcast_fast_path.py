@@ -136,6 +136,9 @@ def test_subnormal_multiply_rounds_t_to_the_code():
     neg = -np.arange(1, 1 << 20, dtype=np.float32) / np.float32(256.0)
     assert np.all(((neg * TINY).view(np.uint32) & 0x80000000) != 0)
     assert (np.float32(-0.0) * TINY).view(np.uint32) == 0x80000000
+    # far below: the product is a negative normal or subnormal, sign bit set all the same
+    far = -np.float32(2.0) ** np.arange(12, 127, dtype=np.float32)
+    assert np.all(((far * TINY).view(np.uint32) & 0x80000000) != 0)
     # halves go to the even neighbour
     for t, r in ((0.5, 0), (1.5, 2), (2.5, 2), (7.5, 8), (125.5, 126), (33.5, 34), (34.5, 34)):
         assert int((np.float32(t) * TINY).view(np.uint32)) == r
