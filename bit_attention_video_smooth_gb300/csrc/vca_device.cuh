@@ -364,26 +364,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return d;
 }
 
-// hi + lo split of x for two bf16 operands: hi = bf16(x), lo = x - hi (exact
-// in fp32; bf16(lo) keeps x to ~16 significant bits).
-__device__ __forceinline__ void split_bf16(float x, float &hi, float &lo) {
-    hi = __bfloat162float(__float2bfloat16_rn(x));
-    lo = __fsub_rn(x, hi);
-}
-// The same split of two values, packed: h = bf16(a) | bf16(b) << 16 and
-// l = bf16(a - hi(a)) | bf16(b - hi(b)) << 16 (one conversion per word; the
-// hi halves are read back as fp32 by placing them in the high 16 bits).
+// hi + lo split of two values for bf16 operands, packed: h = bf16(a) |
+// bf16(b) << 16 and l = bf16(a - hi(a)) | bf16(b - hi(b)) << 16, with
+// hi(x) = bf16(x) (x - hi(x) is exact in fp32; bf16 of it keeps x to ~16
+// significant bits).  One conversion per word; the hi halves are read back as
+// fp32 by placing them in the high 16 bits.
 __device__ __forceinline__ void split_pack_bf16x2(float a, float b, uint32_t &h, uint32_t &l) {
     h = pack_bf16x2(a, b);
     const float ha = __uint_as_float(h << 16), hb = __uint_as_float(h & 0xffff0000u);
     l = pack_bf16x2(__fsub_rn(a, ha), __fsub_rn(b, hb));
 }
 
-// Two fp32 values -> two E4M3 bytes (round to nearest even, saturate to 448);
-// `lo` lands in the low byte.
-__device__ __forceinline__ uint32_t e4m3x2(float lo, float hi) {
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3));
-}
 
 // Four fp32 values -> four E4M3 bytes of one word (byte i = value i; round to
 // nearest even, saturate to 448): two cvt instructions and a register pack.
