@@ -334,12 +334,15 @@ def _prepped_both(V, orc, BH, N, seed, vmode=0):
     return ref, p
 
 
-# N spans one block, two, a ragged few (odd), the longest tail without a
-# mean-restore MMA (19 blocks), the first MMA on the last block (20), two
-# MMAs (32), and a later MMA on the last block (36)
+# N spans one block, two, a ragged few (odd), the longest loop without an
+# in-loop mean-restore MMA (19 blocks: the epilogue adds them as two MMA groups
+# from means buffers 0 and 1), the first in-loop MMA on the last block (20),
+# two MMAs (32), a later MMA on the last block (36), and two-group epilogue
+# tails that start in means buffer 1 (35 blocks) and 0 again (51)
 @pytest.mark.parametrize("expcast", [1, 0])
 @pytest.mark.parametrize("BH,N,seed", [(2, 1024, 0), (1, 128, 1), (1, 256, 5), (3, 384, 2), (2, 640, 6), (1, 2304, 3),
-                                        (1, 2432, 7), (1, 2560, 8), (2, 4096, 4), (1, 4608, 9)])
+                                        (1, 2432, 7), (1, 2560, 8), (2, 4096, 4), (1, 4608, 9), (1, 4480, 10),
+                                        (1, 6528, 11)])
 def test_attention_parity_on_oracle_operands(V, orc, expcast, BH, N, seed):
     ref, p = _prepped_both(V, orc, BH, N, seed)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -351,9 +354,11 @@ def test_attention_parity_on_oracle_operands(V, orc, expcast, BH, N, seed):
     assert rel <= REL_L2 and mx <= MAX_ABS, (rel, mx)
 
 
-# N spans one block, a ragged few, the first mean-restore flush (16 blocks),
-# one block past it (17), and two flushes (32)
-@pytest.mark.parametrize("BH,N,seed", [(1, 128, 21), (3, 384, 22), (2, 2048, 23), (1, 2176, 24), (2, 4096, 25)])
+# N spans one block, a ragged few, 16 blocks, 17 (a two-group epilogue tail),
+# 32 (one in-loop mean-restore MMA), and 35 (a two-group tail from means
+# buffer 1)
+@pytest.mark.parametrize("BH,N,seed", [(1, 128, 21), (3, 384, 22), (2, 2048, 23), (1, 2176, 24), (2, 4096, 25),
+                                        (1, 4480, 26)])
 def test_attention_nvfp4_parity_on_oracle_operands(V, orc, BH, N, seed):
     ref, p = _prepped_both(V, orc, BH, N, seed, vmode=V.VCA_V_NVFP4)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
