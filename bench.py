@@ -199,8 +199,8 @@ def oracle_sample(w, seed: int = 0):
     oracle.build()
     cores = oracle.threads()
     # 1024 query rows per head (always the first and last blocks' edge rows) on
-    # two heads: about 10 s of oracle work on 16 cores at the Wan shape
-    heads = max(1, min(w.BH, 2))
+    # eight heads: about 11 s of oracle work on 16 cores at the Wan shape
+    heads = max(1, min(w.BH, 8))
     rows_per_head = 1024
     sub = I.with_n(w, w.N, H=heads, B=1)
     q, k, v = (I.to_u16(t).reshape(heads, w.N, 128) for t in I.make_qkv(sub, seed=seed))
