@@ -4,7 +4,7 @@
 // head, then Key and Value are permuted together by cluster label).
 //
 // One Lloyd round is two launches:
-//   assign  grid (chunks, BH): each CTA takes kChunkTokens tokens in 128-token
+//   assign  grid (chunks, BH): each CTA takes chunk_tokens tokens in 128-token
 //           tiles (TMA, 128-byte swizzle), forms the tile's dot products with
 //           all centroids on the tensor core (tcgen05, accumulators in TMEM),
 //           assigns each token to its nearest centroid (|c|^2 - 2 v.c in fp32,
@@ -77,7 +77,7 @@ struct AssignLayout {
     static_assert(kBytes <= 232448, "shared memory budget");
 };
 
-// One Lloyd round over a chunk of kChunkTokens tokens of one (batch, head):
+// One Lloyd round over a chunk of chunk_tokens tokens of one (batch, head):
 // assign every token to its nearest centroid and accumulate the chunk's
 // per-cluster sums and counts, both contractions on the tensor core
 // (kind::f16, bf16 operands, fp32 accumulators in TMEM):
@@ -92,7 +92,7 @@ struct AssignLayout {
 //              sums accumulate in TMEM over its tiles in a fixed order.
 template <int KPAD>
 __global__ void __launch_bounds__(kThreads, 1)
-    group_assign_kernel(const __grid_constant__ CUtensorMap tmV, int N, int k, int nchunk, const float *C,
+    group_assign_kernel(const __grid_constant__ CUtensorMap tmV, int N, int k, int nchunk, int chunk_tokens, const float *C,
                         const float *norm, int32_t *labels, float *part_sum, int32_t *part_cnt, int32_t *dev_status,
                         uint64_t limit_ns) {
     using L = AssignLayout<KPAD>;
@@ -115,8 +115,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int chunk = blockIdx.x, bh = blockIdx.y;
-    const int tok0 = chunk * kChunkTokens;
-    const int ntiles = min(kChunkTokens, N - tok0) / kBlk;
+    const int tok0 = chunk * chunk_tokens;
+    const int ntiles = min(chunk_tokens, N - tok0) / kBlk;
     const float *Cb = C + static_cast<int64_t>(bh) * k * kD;
 
     if (tid == 0) {
@@ -349,7 +349,7 @@ __global__ void __launch_bounds__(kBlk) group_reduce_kernel(int k, int nchunk, c
     }
 }
 
-__global__ void __launch_bounds__(32) group_scatter_kernel(int N, int k, int nchunk,
+__global__ void __launch_bounds__(32) group_scatter_kernel(int N, int k, int nchunk, int chunk_tokens,
                                                            const int32_t *__restrict__ labels,
                                                            const int32_t *__restrict__ part_cnt,
                                                            int32_t *__restrict__ perm) {
@@ -365,8 +365,8 @@ __global__ void __launch_bounds__(32) group_scatter_kernel(int N, int k, int nch
         sBase[l] = before + earlier;
     }
     __syncwarp();
-    const int tok0 = chunk * kChunkTokens;
-    const int tok1 = min(N, tok0 + kChunkTokens);
+    const int tok0 = chunk * chunk_tokens;
+    const int tok1 = min(N, tok0 + chunk_tokens);
     const int32_t *lab = labels + static_cast<int64_t>(bh) * N;
     int32_t *out = perm + static_cast<int64_t>(bh) * N;
     for (int t = tok0; t < tok1; t += 32) {
@@ -396,23 +396,52 @@ bool make_v_map(CUtensorMap *map, const uint16_t *V, uint64_t rows) {
 }
 
 template <int KPAD>
-cudaError_t launch_assign(const CUtensorMap &tmV, int BH, int N, int k, int nchunk, const float *C, const float *norm,
-                          int32_t *labels, float *psum, int32_t *pcnt, int32_t *dev_status, uint64_t limit_ns,
-                          cudaStream_t st) {
+cudaError_t launch_assign(const CUtensorMap &tmV, int BH, int N, int k, int nchunk, int chunk_tokens, const float *C,
+                          const float *norm, int32_t *labels, float *psum, int32_t *pcnt, int32_t *dev_status,
+                          uint64_t limit_ns, cudaStream_t st) {
     constexpr uint32_t smem = AssignLayout<KPAD>::kBytes;
     cudaError_t e = cudaFuncSetAttribute(group_assign_kernel<KPAD>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    group_assign_kernel<KPAD><<<dim3(nchunk, BH), kThreads, smem, st>>>(tmV, N, k, nchunk, C, norm, labels, psum,
-                                                                         pcnt, dev_status, limit_ns);
+    group_assign_kernel<KPAD><<<dim3(nchunk, BH), kThreads, smem, st>>>(tmV, N, k, nchunk, chunk_tokens, C, norm,
+                                                                         labels, psum, pcnt, dev_status, limit_ns);
     return cudaGetLastError();
 }
 
 }  // namespace
 
+// Chunks per head for the assign kernel: the count c that minimises the
+// launch's modelled makespan, ceil(BH c / SMs) waves of ceil(tiles / c) + 3
+// tile times each (3 for a CTA's fixed start-up and drain), with at least 8
+// tiles per chunk; ties go to fewer chunks.  For B=1, H=40, N=70,656 that is
+// 15 chunks of 37 tiles (4 waves of 152 CTAs but 8 slots) instead of 18 of 32
+// (a fifth, partly filled wave).
+constexpr int kSmCount = 152;
+constexpr int kMinChunkTiles = 8;
+constexpr int kChunkStartTiles = 3;
+static int group_chunks_per_head(int BH, int tiles) {
+    int best = 1;
+    long best_cost = -1;
+    for (int c = 1; c <= tiles; ++c) {
+        const int per = (tiles + c - 1) / c;
+        if (per < kMinChunkTiles && c > 1) break;
+        if ((tiles + per - 1) / per != c) continue;   // c chunks of `per` tiles must all be non-empty
+        const long waves = (static_cast<long>(BH) * c + kSmCount - 1) / kSmCount;
+        const long cost = waves * (per + kChunkStartTiles);
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = c;
+        }
+    }
+    return best;
+}
+
 GroupWorkspace group_workspace_layout(int BH, int N, int k) {
     GroupWorkspace w;
-    w.nchunk = (N + kChunkTokens - 1) / kChunkTokens;
+    const int tiles = (N + kBlk - 1) / kBlk;
+    const int c = group_chunks_per_head(BH, tiles);
+    w.chunk_tokens = ((tiles + c - 1) / c) * kBlk;
+    w.nchunk = (N + w.chunk_tokens - 1) / w.chunk_tokens;
     size_t off = 0;
     auto take = [&](size_t bytes) { size_t o = off; off += (bytes + 255) & ~size_t(255); return o; };
     w.off_centroids = take(sizeof(float) * BH * k * kD);
@@ -440,14 +469,16 @@ cudaError_t launch_group(const uint16_t *V, int BH, int N, int k, int iters, int
     if (e != cudaSuccess) return e;
     for (int it = 0; it < iters; ++it) {
         e = (k <= 64)
-                ? launch_assign<64>(tmV, BH, N, k, w.nchunk, C, norm, labels, psum, pcnt, dev_status, limit_ns, st)
-                : launch_assign<128>(tmV, BH, N, k, w.nchunk, C, norm, labels, psum, pcnt, dev_status, limit_ns, st);
+                ? launch_assign<64>(tmV, BH, N, k, w.nchunk, w.chunk_tokens, C, norm, labels, psum, pcnt, dev_status,
+                                    limit_ns, st)
+                : launch_assign<128>(tmV, BH, N, k, w.nchunk, w.chunk_tokens, C, norm, labels, psum, pcnt, dev_status,
+                                     limit_ns, st);
         if (e != cudaSuccess) return e;
         group_reduce_kernel<<<dim3(k, BH), kBlk, 0, st>>>(k, w.nchunk, psum, pcnt, C, norm, counts);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
-    group_scatter_kernel<<<dim3(w.nchunk, BH), 32, 0, st>>>(N, k, w.nchunk, labels, pcnt, perm);
+    group_scatter_kernel<<<dim3(w.nchunk, BH), 32, 0, st>>>(N, k, w.nchunk, w.chunk_tokens, labels, pcnt, perm);
     return cudaGetLastError();
 }
 

@@ -8,11 +8,13 @@
 
 namespace vca {
 
-constexpr int kChunkTokens = 4096;   // tokens per CTA in the k-means assign kernel
 constexpr int kMaxK = 128;           // largest supported cluster count
 
+// The k-means assign kernel's work split: each CTA takes one chunk of
+// chunk_tokens tokens (a multiple of 128) of one (batch, head), nchunk chunks
+// per head (the last one ragged); group_workspace_layout picks the split.
 struct GroupWorkspace {
-    int nchunk;
+    int nchunk, chunk_tokens;
     size_t off_centroids, off_norm, off_psum, off_pcnt, bytes;
 };
 GroupWorkspace group_workspace_layout(int BH, int N, int k);

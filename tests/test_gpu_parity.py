@@ -82,7 +82,7 @@ def test_e4m3_hardware_conversion_matches_oracle_everywhere(V, orc):
 # ---------------------------------------------------------------------------
 # group: k-means + stable permutation
 # ---------------------------------------------------------------------------
-# sizes span one token tile, several 4096-token chunks with a ragged last one,
+# sizes span one token tile, several assign chunks with a ragged last one,
 # and the cluster counts of both kernel variants (k <= 64, k <= 128)
 @pytest.mark.parametrize("BH,N,k,iters", [(2, 1024, 8, 10), (3, 2 * 4096 + 384, 16, 4), (1, 256, 1, 2),
                                           (2, 2048, 64, 8), (1, 512, 128, 3), (1, 4096 + 128, 100, 5)])
