@@ -411,14 +411,16 @@ cudaError_t launch_assign(const CUtensorMap &tmV, int BH, int N, int k, int nchu
 }  // namespace
 
 // Chunks per head for the assign kernel: the count c that minimises the
-// launch's modelled makespan, ceil(BH c / SMs) waves of ceil(tiles / c) + 3
-// tile times each (3 for a CTA's fixed start-up and drain), with at least 8
+// launch's modelled makespan, ceil(BH c / SMs) waves of ceil(tiles / c) + 6
+// tile times each (6 for a CTA's fixed start-up -- centroid staging, the first
+// V tile's latency -- and its drain of the partial sums), with at least 8
 // tiles per chunk; ties go to fewer chunks.  For B=1, H=40, N=70,656 that is
-// 15 chunks of 37 tiles (4 waves of 152 CTAs but 8 slots) instead of 18 of 32
-// (a fifth, partly filled wave).
+// 7 chunks of 79 tiles (280 CTAs, two waves); measured there: 7 chunks
+// 1.48 ms per group step, 11: 1.50, 15: 1.52, 18 (4096 tokens each, a fifth
+// partly filled wave): 1.66.
 constexpr int kSmCount = 152;
 constexpr int kMinChunkTiles = 8;
-constexpr int kChunkStartTiles = 3;
+constexpr int kChunkStartTiles = 6;
 static int group_chunks_per_head(int BH, int tiles) {
     int best = 1;
     long best_cost = -1;

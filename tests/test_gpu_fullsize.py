@@ -119,7 +119,7 @@ def test_fullsize_k_smooth_prep(V, orc):
 
 
 def test_fullsize_group_bit_exact_on_separated_clusters(V, orc):
-    """The group at the Wan shape (B=1, H=40, N=70,656, k=64, 8 rounds: 15
+    """The group at the Wan shape (B=1, H=40, N=70,656, k=64, 8 rounds: 7
     token chunks per head, the launch configuration of the full workload) on
     well-separated clusters: labels, permutation and counts of sampled heads
     bit-exact against the oracle."""
