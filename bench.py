@@ -440,10 +440,11 @@ def run_ours(args, w, ws, rank, local):
 
 
 def other_configs(args, p, w, status, stream):
-    """Attention alone on the other two single-GPU configurations, timed in the
+    """Attention alone on the other single-GPU configurations, timed in the
     same process after the step: the Wan shape with ExpCast off (the exp path,
-    on the step's prepared operands) and the NVFP4 workload (its own inputs,
-    grouped and prepared once)."""
+    on the step's prepared operands), the NVFP4 workload and the sequence-length
+    sweep's other points (each with its own inputs, grouped and prepared
+    once)."""
     import torch
     from bit_attention_video_smooth_gb300 import inputs as I
     from bit_attention_video_smooth_gb300 import vca
@@ -487,6 +488,18 @@ def other_configs(args, p, w, status, stream):
                                                          dev_status=status)))
     del Q, K, V, g, p4, O4
     torch.cuda.empty_cache()
+    # the N sweep at B=1, H=40 (N = 70,656 is the step itself)
+    for n in (4096, 16384, 32768, 131072):
+        ws = I.with_n(I.WORKLOADS["sweep"], n)
+        Q, K, V = I.make_qkv(ws, seed=4321 + n, device=p.q8.device)
+        g = vca.group(V, ws.k, ws.iters)
+        ps = vca.prep_quant(Q, K, V, g.perm, vca.VCA_V_E4M3)
+        del Q, K, V, g
+        Os = torch.empty((ws.B, ws.H, ws.N, 128), dtype=torch.bfloat16, device=p.q8.device)
+        out[ws.name] = entry(ws, timed(lambda: vca.attention(ps, ws.B, ws.H, ws.N, expcast=ws.expcast, out=Os,
+                                                             dev_status=status)))
+        del ps, Os
+        torch.cuda.empty_cache()
     return out
 
 
